@@ -1,0 +1,474 @@
+"""Benchmark of the fused P-EAGLE drafting step (verify + rebuild + assemble).
+
+One step = one pe_step launch over one batch of seeded synthetic inputs
+already resident in HBM.  Default workload: large-batch decode, B=256 requests,
+K'=7, K=7, H=2048, V=151936, bf16 (the configuration whose HBM-bandwidth
+target is stated).  Prints ONE JSON line on rank 0.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+  python bench.py --impl reference ...   # the CPU oracle, same metric
+
+Timing: W untimed steps, then K steps, each bracketed by CUDA events on the
+launching stream; between steps the L2 is flushed by writing a buffer of
+twice its size (outside the events).  Multi-GPU (torchrun): every rank runs
+its own independent requests (weak scaling, no collective on the data path);
+the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from speculative_decoding_pe_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "verify+rebuild+assemble draft rows/s"
+UNIT = "rows/s"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ("speculative_decoding_pe_gb300/csrc/pe_step.cu",
+                  "speculative_decoding_pe_gb300/csrc/pe_internal.cuh",
+                  "speculative_decoding_pe_gb300/csrc/pe_workspace.cuh")
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(world: int, backend: str):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """Largest value of ``x`` across ranks (the timing reduction)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(x: float, world: int, device) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def rank_seed(workload: str, rank: int) -> int:
+    """Each rank draws its own independent requests."""
+    return 5000 + 97 * (list(wl.SPECS).index(workload) + 1) + rank
+
+
+# ------------------------------------------------------------ byte counts
+
+def algorithmic_bytes(spec: wl.WorkloadSpec, R: int) -> dict:
+    """Bytes one step must move at minimum (each byte counted once).
+
+    logits: every row read once; hidden: every target row read once;
+    emb: one table row per verified / prompt slot plus the MASK row (the
+    repeated MASK-row reads hit L2); X: written once; metadata: 18 bytes per
+    output slot (token, position, two masks, slot id) plus the per-row and
+    per-request integers."""
+    B, Kp, K, V, H = spec.B, spec.Kp, spec.K, spec.V, spec.H
+    elt = torch.tensor([], dtype=spec.dtype).element_size()
+    Rl = B * (Kp + 1)
+    T = R + B * (K - 1)
+    parts = {
+        "logits": Rl * V * elt,
+        "hidden": R * H * elt,
+        "emb": (R + 1) * H * elt,
+        "X": T * 2 * H * elt,
+        "metadata": 18 * T + 12 * R + 4 * (B + 1) + 8 * B + 4 * B * K + 4 * Rl,
+    }
+    parts["total"] = sum(parts.values())
+    return parts
+
+
+def measured_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch from the committed ncu summary of this kernel and
+    workload, or None when there is none or the kernel changed since."""
+    path = os.path.join(ROOT, "profiles", "pe_step_%s.md" % workload)
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_hash = re.search(r"kernel_source_sha256_16\s*=\s*([0-9a-f]+)", text)
+    m_bytes = re.search(r"dram_bytes_per_launch\s*=\s*([0-9]+)", text)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_bytes.group(1))
+
+
+# ------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,"
+             "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        self.windows = []
+
+    def mark(self):
+        return time.time()
+
+    def stop(self, t0: float, t1: float) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        out, _ = self.proc.communicate(timeout=10)
+        rows = []
+        for rec in csv.reader(io.StringIO(out)):
+            if len(rec) < 10:
+                continue
+            try:
+                ts = time.mktime(time.strptime(rec[0].strip().split(".")[0],
+                                               "%Y/%m/%d %H:%M:%S"))
+                rows.append((ts, [r.strip() for r in rec]))
+            except ValueError:
+                continue
+        inside = [r for ts, r in rows if t0 - 1.0 <= ts <= t1 + 1.0] or [r for _, r in rows]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[2]) for r in inside if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in inside if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in inside for i in range(4)
+                          if r[6 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(inside)}
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def sub_workload(w, nreq: int):
+    """The first ``nreq`` requests of a workload, on the host."""
+    import dataclasses
+    spec = w.spec.with_(B=nreq)
+    rows = nreq * (w.Kp + 1)
+    if w.in_offsets is not None:
+        R = int(w.in_offsets[nreq])
+        offs = w.in_offsets[:nreq + 1].cpu()
+    else:
+        R = rows
+        offs = None
+    return dataclasses.replace(
+        w, spec=spec, logits=w.logits[:rows].cpu().contiguous(), in_offsets=offs,
+        in_tokens=w.in_tokens[:R].cpu(), in_positions=w.in_positions[:R].cpu(),
+        block_table=w.block_table[:nreq].cpu(), emb=w.emb.cpu(), hidden=w.hidden[:R].cpu(),
+        h_shared=w.h_shared.cpu(), planted_accept=w.planted_accept[:nreq],
+        planted_bonus=w.planted_bonus[:nreq])
+
+
+def time_oracle(sub, budget_s: float, min_runs: int = 1):
+    """Run the oracle step on ``sub`` until ``budget_s`` seconds have passed."""
+    import oracle
+    times = []
+    start = time.perf_counter()
+    while len(times) < min_runs or time.perf_counter() - start < budget_s:
+        t0 = time.perf_counter()
+        oracle.step(sub)
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def pick_sample_requests(w, per_step_s: float) -> int:
+    probe = sub_workload(w, 1)
+    t = min(time_oracle(probe, 0.0, min_runs=2))
+    return max(1, min(w.B, int(per_step_s / max(t, 1e-6))))
+
+
+def cpu_model() -> str:
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+# ------------------------------------------------------------ arms
+
+def config_of(spec, extra=None) -> dict:
+    c = {"workload": spec.name, "description": spec.description, "B": spec.B,
+         "Kp": spec.Kp, "K": spec.K, "H": spec.H, "V": spec.V,
+         "dtype": str(spec.dtype).replace("torch.", ""),
+         "l2": "flushed between timed steps (write of 2x L2)",
+         "parallelism": "requests sharded across ranks, no data-path collective"}
+    if extra:
+        c.update(extra)
+    return c
+
+
+def run_reference(args):
+    rank, world, local = dist_env()
+    if rank != 0:
+        return 0
+    spec = wl.SPECS[args.workload]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    w = wl.make_workload(spec, rank_seed(args.workload, 0), device=dev)
+    per_step = min(1.0, 120.0 / max(1, args.steps + args.warmup))
+    nreq = pick_sample_requests(w, per_step)
+    sub = sub_workload(w, nreq)
+    import oracle
+    for _ in range(args.warmup):
+        oracle.step(sub)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.step(sub)
+    dt = (time.perf_counter() - t0) / max(1, args.steps)
+    T = sub.R + nreq * (spec.K - 1)
+    value = T / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype":
+        str(spec.dtype).replace("torch.", ""), "data": "synthetic",
+        "config": config_of(spec),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "first %d of %d requests per step (%d draft rows), "
+                                   "single-threaded C oracle on %s" % (
+                                       nreq, spec.B, T, cpu_model())},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args):
+    rank, world, local = dist_env()
+    if world != args.gpus:
+        raise SystemExit("--gpus %d but WORLD_SIZE=%d" % (args.gpus, world))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    from speculative_decoding_pe_gb300 import _native, harness
+    _native.load()  # fails loudly when the CUDA library is missing
+    if args.tuning:
+        _native.set_tuning(**json.loads(args.tuning))
+
+    spec = wl.SPECS[args.workload]
+    w = wl.make_workload(spec, rank_seed(args.workload, rank), device=device)
+    out, ws, err = harness.allocate(w, device)
+    packed = harness.pack(w, out, ws, err)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        _native.step_packed(packed, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(device)
+    if int(err.item()) != 0:
+        raise SystemExit("device error word %d on warm-up" % int(err.item()))
+
+    sampler = ClockSampler(local)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(device)
+    t_wall0 = time.time()
+    torch.cuda.nvtx.range_push("timed")
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize(device)
+    barrier(world)
+    t_wall1 = time.time()
+    clocks = sampler.stop(t_wall0, t_wall1)
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    mean_ms = sum(step_ms) / len(step_ms)
+    mean_ms_max = max_over_ranks(mean_ms, world, device)
+
+    T = w.T
+    rows_all = sum_over_ranks(float(T), world, device)
+    value = rows_all / (mean_ms_max / 1e3)
+
+    bytes_ = algorithmic_bytes(spec, w.R)
+    peak, peak_kind = measured_peak()
+    achieved = bytes_["total"] / (mean_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
+                "peak_source": peak_kind, "algorithmic_bytes_per_launch": bytes_["total"],
+                "kernel": "pe::step_kernel<bf16>" if spec.dtype == torch.bfloat16
+                else "pe::step_kernel<f32>"}
+
+    e2e = measure_e2e(w, out, ws, err, packed, stream, device, args) if args.e2e else None
+    if e2e is not None:
+        e2e_ms = max_over_ranks(e2e["ms"], world, device)
+        e2e = {"value": rows_all / (e2e_ms / 1e3), "unit": UNIT,
+               "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
+               "ms_per_step": e2e_ms}
+
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_baseline:
+        cpu = measure_cpu_baseline(w, args.cpu_budget)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": str(spec.dtype).replace("torch.", ""), "data": "synthetic",
+            "config": config_of(spec, {"T_per_rank": T, "R_per_rank": w.R,
+                                       "median_us": statistics.median(step_ms) * 1e3,
+                                       "min_us": min(step_ms) * 1e3,
+                                       "tuning": _native.get_tuning()}),
+            "us_per_step": mean_ms_max * 1e3,
+            "hbm_gbs": achieved,
+            "roofline": roofline,
+            "e2e": e2e,
+            "cpu_baseline": cpu,
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def measure_e2e(w, out, ws, err, packed, stream, device, args):
+    """The same step through the public API with inputs copied in from pinned
+    host memory and the per-request results copied back, every step."""
+    from speculative_decoding_pe_gb300 import _native
+    per_step = [w.logits, w.hidden, w.in_tokens, w.in_positions]
+    if w.in_offsets is not None:
+        per_step.append(w.in_offsets)
+    host = []
+    for t in per_step:
+        if t.dim() == 2 and t.stride(0) != t.shape[1]:
+            base = t.as_strided((t.shape[0], t.stride(0)), (t.stride(0), 1))
+            host.append((base, base.cpu().pin_memory()))
+        else:
+            host.append((t, t.cpu().pin_memory()))
+    res_dev = [out.accepted_len, out.bonus_token]
+    res_host = [torch.empty_like(r, device="cpu").pin_memory() for r in res_dev]
+    h2d = sum(h.numel() * h.element_size() for _, h in host)
+    d2h = sum(r.numel() * r.element_size() for r in res_host)
+    n = max(3, min(args.steps, args.e2e_steps))
+
+    def one():
+        for d, h in host:
+            d.copy_(h, non_blocking=True)
+        _native.step_packed(packed, stream)
+        for d, h in zip(res_dev, res_host):
+            h.copy_(d, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    return {"ms": e0.elapsed_time(e1) / n, "h2d": h2d, "d2h": d2h}
+
+
+def measure_cpu_baseline(w, budget_s: float):
+    nreq = pick_sample_requests(w, budget_s / 20)
+    sub = sub_workload(w, nreq)
+    times = time_oracle(sub, budget_s, min_runs=3)
+    T = sub.R + nreq * (w.K - 1)
+    t = statistics.median(times)
+    return {"value": T / t, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "first %d of %d requests (%d draft rows), %d runs, median %.1f ms, "
+                      "single-threaded C oracle on %s" % (
+                          nreq, w.B, T, len(times), t * 1e3, cpu_model())}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__,
+                                 formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=list(wl.SPECS), default="decode_b256")
+    ap.add_argument("--tuning", default="", help="JSON launch-shape knobs")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-e2e", dest="e2e", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        raise SystemExit("--warmup must be at least 3")
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,214 @@
+/*
+ * pe_api.h -- C ABI of libpe.so: the per-step data path of P-EAGLE parallel
+ * drafting on one GB300 (sm_103a): greedy verification, the fused
+ * draft-batch rebuild and the drafter input assembly.
+ *
+ * Sources (page title -- section):
+ *  [P1] "P-EAGLE: Faster LLM Inference with Parallel Speculative Decoding in
+ *       vLLM" -- quick-read section (equation Input_i; acceptance length;
+ *       rejected tokens mapped to -1) and the vLLM engineering listing
+ *       (target hidden rows scattered to new slots, then MASK slots
+ *       overwritten with the learned hidden state).
+ *  [P2] "P-EAGLE: Parallel Speculative Decoding in vLLM" -- Step 2: Parallel
+ *       Drafting; Fused Triton Kernel; Hidden State Management; KV Cache and
+ *       CUDA Graphs.
+ *
+ * Notation.  Request b in [0,B).  Its target (verification) segment holds
+ * n_b rows starting at input offset io_b; decode has n_b = K'+1 (the last
+ * committed token, then drafts d_1..d_K'), the first step after prefill has
+ * K' = 0 and n_b = prompt length.  Its output segment holds m_b = n_b+K-1
+ * rows at output offset oo_b.  R = sum n_b, T = sum m_b = R + B(K-1).
+ * The Kp+1 "verified rows" of a segment are its last Kp+1 rows; logits hold
+ * exactly those rows, request-major: logits row b(Kp+1)+j.
+ *
+ * Conventions shared by every entry point:
+ *  - All pointers not marked "host" are device pointers.  The caller owns
+ *    every buffer; the library never allocates, frees or synchronises, and
+ *    enqueues its work on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream).  Outputs are valid once the stream reaches that point.
+ *  - The return value reports host-checkable argument errors only
+ *    (pe_status); nothing is enqueued when it is not PE_OK.
+ *  - Data errors found on the device never trap: the kernel ORs a PE_ERR_*
+ *    bit into *err (a device word the caller zeroes and reads when it wants
+ *    to) and writes the defined value stated for that case.
+ *  - Integer outputs are exact.  Floating point only enters the argmax:
+ *    values are compared numerically (-0.0 == +0.0), the lowest column wins
+ *    ties; logits must not hold NaN.
+ *  - Element types: PE_F32 (4 bytes) or PE_BF16 (2 bytes).  Embedding table,
+ *    target hidden rows, h_shared and X share one element type.
+ *  - Alignment: logits base, emb, target_hidden, h_shared and X must be
+ *    16-byte aligned, the logits row stride (in bytes) and H*elt a multiple
+ *    of 16 bytes; otherwise PE_EALIGN.
+ */
+#ifndef PE_API_H
+#define PE_API_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum pe_status {
+  PE_OK = 0,
+  PE_EINVAL = -1, /* NULL pointer, size out of range, inconsistent sizes */
+  PE_EDTYPE = -2, /* element type is neither PE_F32 nor PE_BF16 */
+  PE_EALIGN = -3, /* pointer / stride / row size not 16-byte aligned */
+  PE_ECUDA = -4   /* the CUDA runtime reported an error at launch */
+} pe_status;
+
+typedef enum pe_dtype { PE_F32 = 0, PE_BF16 = 1 } pe_dtype;
+
+/* Bits of the device error word. */
+#define PE_ERR_TOKEN_RANGE 1u /* gathered token id outside [0,V): zero row   */
+#define PE_ERR_BLOCK_RANGE 2u /* pos < 0 or pos/block_size >= bt_width: -1  */
+#define PE_ERR_SLOT_RANGE 4u  /* accepted_len outside [0,Kp]: taken as 0    */
+#define PE_ERR_OFFSETS 8u     /* in_offsets invalid: nothing is written     */
+#define PE_ERR_MAP_RANGE 16u  /* hidden_map entry outside [0,T): skipped    */
+
+/* Limits checked on the host. */
+#define PE_MAX_KP 255 /* previous draft depth K'  */
+#define PE_MAX_K 256  /* new draft depth K        */
+
+/* Bytes of scratch that pe_verify_greedy / pe_step need for a batch with
+ * `logits_rows` = B*(Kp+1) logits rows and B requests.  The caller
+ * allocates it once, zero-filled, and may reuse it for every later call of
+ * any size up to those; each call leaves it zeroed again on completion.
+ * Calls that may run concurrently need separate workspaces. */
+size_t pe_workspace_bytes(int32_t logits_rows, int32_t B);
+
+/* Greedy verification [P1 quick-read: acceptance length].
+ *  logits      [B*(Kp+1), V] of `dtype`, row stride `row_stride` elements.
+ *  in_tokens   [B*(Kp+1)] int32: row b(Kp+1)+j+1 holds draft d_{j+1} of
+ *              request b (row b(Kp+1) holds the last committed token and is
+ *              not read).  May be NULL when Kp == 0.
+ *  accepted_len[B] out: a_b = first j < Kp with argmax(row j) != d_{j+1},
+ *              or Kp when every draft matches.
+ *  bonus_token [B] out: argmax of row a_b (the target's own next token).
+ *  target_argmax [B*(Kp+1)] out, or NULL: every row's argmax.
+ *  workspace   pe_workspace_bytes(B*(Kp+1), B) bytes, zeroed (see above).
+ *  err         device error word (no bits are defined for this call).
+ * B == 0 enqueues nothing. */
+int pe_verify_greedy(const void* logits, int dtype, int64_t row_stride,
+                     int32_t B, int32_t Kp, int32_t V, const int32_t* in_tokens,
+                     int32_t* accepted_len, int32_t* bonus_token,
+                     int32_t* target_argmax, void* workspace, uint32_t* err,
+                     void* stream);
+
+/* Draft-batch rebuild [P2 Fused Triton Kernel; KV Cache and CUDA Graphs].
+ * For request b with bonus slot s_b = n_b-1-Kp+a_b and slot k of its output
+ * segment (t = oo_b + k):
+ *   k <  s_b        token in[io_b+k+1] (shift by one), position pos[io_b+k]
+ *   k == s_b        token bonus_b (next-token prediction), position pos[io_b+s_b]
+ *   s_b < k < n_b   rejected: is_rejected=1, position pos[io_b+k], token
+ *                   in[io_b+k+1] for k < n_b-1 and mask_id for k = n_b-1
+ *   n_b <= k < m_b  MASK: is_masked=1, token mask_id,
+ *                   position pos[io_b+s_b] + (k-n_b+1)
+ *   slot_mapping[t] = -1 when rejected, else
+ *     block_table[b*bt_width + pos/block_size]*block_size + pos%block_size
+ *     (-1 and PE_ERR_BLOCK_RANGE when pos < 0 or pos/block_size >= bt_width)
+ *   hidden_map[io_b+k] = oo_b+k for k < n_b
+ *   sample_idx[b*K + 0] = oo_b+s_b, sample_idx[b*K + i] = oo_b+n_b+i-1
+ *   out_offsets[b] = oo_b (exclusive scan of m_b), out_offsets[B] = T
+ *  in_offsets  [B+1] int32, or NULL for fixed segments n_b = Kp+1 (decode).
+ *              When given: in_offsets[0] = 0, in_offsets[B] = R and every
+ *              n_b >= Kp+1, else PE_ERR_OFFSETS and nothing is written.
+ *  R           total input rows (host): B*(Kp+1) when in_offsets is NULL.
+ *  in_tokens, in_positions [R] int32.
+ *  accepted_len [B] int32 (NULL: all 0); values outside [0,Kp] count as 0
+ *              and raise PE_ERR_SLOT_RANGE.
+ *  bonus_token [B] int32.
+ *  block_table [B, bt_width] int32 physical block ids.
+ *  outputs: out_offsets[B+1], out_tokens[T], out_positions[T] int32;
+ *           is_rejected[T], is_masked[T] uint8; hidden_map[R] int32;
+ *           slot_mapping[T] int64; sample_idx[B*K] int32 or NULL. */
+int pe_build_draft_batch(int32_t B, int32_t Kp, int32_t K, int32_t mask_id,
+                         int32_t R, const int32_t* in_offsets,
+                         const int32_t* in_tokens, const int32_t* in_positions,
+                         const int32_t* accepted_len, const int32_t* bonus_token,
+                         const int32_t* block_table, int32_t bt_width,
+                         int32_t block_size, int32_t* out_offsets,
+                         int32_t* out_tokens, int32_t* out_positions,
+                         uint8_t* is_rejected, uint8_t* is_masked,
+                         int32_t* hidden_map, int64_t* slot_mapping,
+                         int32_t* sample_idx, uint32_t* err, void* stream);
+
+/* Drafter input assembly [P1 equation Input_i and the engineering listing;
+ * P2 Hidden State Management].
+ *   X[t, 0:H]  = emb[out_tokens[t]]   (zeros + PE_ERR_TOKEN_RANGE when the
+ *                token is outside [0,V))
+ *   X[t, H:2H] = h_shared                         when is_masked[t]
+ *              = target_hidden[i] with hidden_map[i] == t   otherwise
+ * i.e. the target rows are scattered through hidden_map and the masked slots
+ * then take h_shared.  hidden_map must not repeat a slot; entries outside
+ * [0,T) are skipped with PE_ERR_MAP_RANGE; an unmasked slot that no entry
+ * names keeps its previous hidden half.
+ *  emb [V,H], target_hidden [R,H], h_shared [H], X [T,2H] of `dtype`;
+ *  out_tokens[T], hidden_map[R] int32; is_masked[T] uint8. */
+int pe_assemble_draft_inputs(int dtype, int32_t H, int32_t V, int32_t T,
+                             int32_t R, const void* emb,
+                             const void* target_hidden, const void* h_shared,
+                             const int32_t* out_tokens,
+                             const int32_t* hidden_map,
+                             const uint8_t* is_masked, void* X, uint32_t* err,
+                             void* stream);
+
+/* The whole step in one launch: pe_verify_greedy, then pe_build_draft_batch
+ * on its result, then pe_assemble_draft_inputs, with identical outputs.
+ * Kp >= 1: decode; in_offsets must be NULL, R = B*(Kp+1).
+ * Kp == 0: first drafting step after prefill; in_offsets [B+1] required,
+ * logits hold one row per request (its last prompt row), whose argmax is
+ * the new token placed at the next-token-prediction slot.
+ * Optional outputs (may be NULL): target_argmax, sample_idx. */
+typedef struct pe_step_args {
+  int32_t B, Kp, K, V, H, R;
+  int32_t mask_id, bt_width, block_size;
+  int32_t logits_dtype, x_dtype;
+  int64_t logits_row_stride; /* elements */
+  /* inputs */
+  const void* logits;
+  const int32_t* in_offsets;
+  const int32_t* in_tokens;
+  const int32_t* in_positions;
+  const int32_t* block_table;
+  const void* emb;
+  const void* target_hidden;
+  const void* h_shared;
+  /* outputs */
+  int32_t* accepted_len;
+  int32_t* bonus_token;
+  int32_t* target_argmax;
+  int32_t* out_offsets;
+  int32_t* out_tokens;
+  int32_t* out_positions;
+  uint8_t* is_rejected;
+  uint8_t* is_masked;
+  int32_t* hidden_map;
+  int64_t* slot_mapping;
+  int32_t* sample_idx;
+  void* X;
+  /* scratch and error word */
+  void* workspace; /* pe_workspace_bytes(B*(Kp+1), B), zeroed */
+  uint32_t* err;
+} pe_step_args;
+
+int pe_step(const pe_step_args* args /* host */, void* stream);
+
+/* Launch-shape knobs of the fused step (process-wide; defaults chosen by
+ * measurement).  Zero fields keep the current value. */
+typedef struct pe_tuning {
+  int32_t ctas_per_sm;     /* resident CTAs per SM for the persistent grid */
+  int32_t chunk_batches;   /* max 32 KiB load batches per argmax unit      */
+  int32_t rows_per_unit;   /* X rows per copy unit                         */
+} pe_tuning;
+int pe_get_tuning(pe_tuning* out /* host */);
+int pe_set_tuning(const pe_tuning* in /* host */);
+
+/* Human-readable name of a pe_status value. */
+const char* pe_status_str(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PE_API_H */

@@ -1,0 +1,109 @@
+// Internal helpers of libpe.so (device and host).  Not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pe_api.h"
+
+namespace pe {
+
+// ---------------------------------------------------------------- launch shape
+constexpr int kThreads = 256;                 // threads per CTA, every kernel
+constexpr int kWarps = kThreads / 32;
+constexpr int kVecPerThread = 8;              // 16-byte loads per thread per batch
+constexpr int kBatchVecs = kThreads * kVecPerThread;  // 2048 vectors = 32 KiB
+constexpr int kMaxRowsPerUnit = 16;           // X rows per copy unit (upper bound)
+
+// ------------------------------------------------------------- element access
+// bf16 is by definition the high half of an IEEE-754 binary32, so widening is
+// a shift; both halves of a 32-bit word hold one element each (low = first).
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// Lane-wise maximum of two pairs of bf16 values (returns one of the inputs,
+// so it is exact).
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t d;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+  return d;
+}
+
+// Total order on non-NaN floats as unsigned integers, with -0.0 == +0.0.
+__device__ __forceinline__ uint32_t ordered_bits(float f) {
+  uint32_t b = __float_as_uint(f);
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+
+// (value, column) packed so that the unsigned maximum is the largest value
+// and, among equal values, the lowest column.  0 is below every real key.
+__device__ __forceinline__ unsigned long long make_key(float v, uint32_t col) {
+  return ((unsigned long long)ordered_bits(v) << 32) |
+         (unsigned long long)(0xffffffffu - col);
+}
+__device__ __forceinline__ uint32_t key_col(unsigned long long k) {
+  return 0xffffffffu - (uint32_t)k;
+}
+
+__device__ __forceinline__ unsigned long long warp_max_key(unsigned long long k) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    unsigned long long x = __shfl_xor_sync(0xffffffffu, k, o);
+    k = x > k ? x : k;
+  }
+  return k;
+}
+
+// ------------------------------------------------------------------ KV slots
+// Paged-KV slot of a kept position; -1 (and an error bit) outside the table.
+__device__ __forceinline__ long long kv_slot(const int32_t* block_table,
+                                             int bt_width, int block_size, int b,
+                                             int pos, uint32_t* err) {
+  if (pos < 0 || pos / block_size >= bt_width) {
+    atomicOr(err, PE_ERR_BLOCK_RANGE);
+    return -1;
+  }
+  long long blk = __ldg(block_table + (long long)b * bt_width + pos / block_size);
+  return blk * block_size + pos % block_size;
+}
+
+// True in every thread of the CTA when in_offsets is a valid partition of R
+// rows into B segments of at least min_rows rows each.
+__device__ __forceinline__ bool offsets_valid(const int32_t* io, int B, int R,
+                                              int min_rows) {
+  int bad = 0;
+  for (int b = threadIdx.x; b <= B; b += blockDim.x) {
+    int v = __ldg(io + b);
+    if (b == 0 && v != 0) bad = 1;
+    if (b == B && v != R) bad = 1;
+    if (b < B && __ldg(io + b + 1) - v < min_rows) bad = 1;
+  }
+  return !__syncthreads_or(bad);
+}
+
+}  // namespace pe
+
+// ------------------------------------------------------------------ host side
+namespace pe_host {
+
+struct DeviceInfo {
+  int sm_count;
+};
+// SM count of the current device (cached per device; no synchronisation).
+int device_info(DeviceInfo* out);
+
+struct Tuning {
+  int ctas_per_sm;
+  int chunk_batches;
+  int rows_per_unit;
+};
+Tuning tuning();
+
+inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+inline int elt_size(int dtype) { return dtype == PE_F32 ? 4 : dtype == PE_BF16 ? 2 : 0; }
+inline int launch_status() {
+  return cudaGetLastError() == cudaSuccess ? PE_OK : PE_ECUDA;
+}
+
+}  // namespace pe_host

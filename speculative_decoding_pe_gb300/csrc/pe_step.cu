@@ -1,0 +1,653 @@
+// Fused P-EAGLE drafting step on one GPU: greedy verification, draft-batch
+// rebuild and drafter input assembly in a single persistent launch
+// (pe_step), and verification alone (pe_verify_greedy).
+//
+// Sources (page title -- section):
+//  "P-EAGLE: Parallel Speculative Decoding in vLLM" -- Fused Triton Kernel
+//    (copy token ids / positions, insert the bonus token, fill MASK slots,
+//    emit rejected / masked masks and the hidden-state mapping in one pass);
+//    Hidden State Management (target rows to their new slots, learned hidden
+//    state broadcast into MASK slots); KV Cache and CUDA Graphs (rejected
+//    slots -> -1).
+//  "P-EAGLE: Faster LLM Inference with Parallel Speculative Decoding in
+//    vLLM" -- quick-read section: Input_1 = emb(new) (+) h_context,
+//    Input_i = emb(mask) (+) h_shared for 2 <= i <= K; acceptance length.
+//
+// Design (one launch, no grid-wide barrier, no spin-wait):
+//  * A persistent grid pulls work units from a counter in the workspace.
+//    Units [0, n_arg) are argmax chunks (row r, chunk c) of the logits, in
+//    row order; units [n_arg, n_units) copy tiles of X rows.
+//  * Argmax chunk: 256 threads stream 32 KiB batches with 16-byte loads
+//    (eight per thread in flight), keep the thread's running maximum and the
+//    column where it first appears, reduce (value, column) keys with warp
+//    shuffles, and merge into the row's key with one 64-bit atomicMax.
+//  * The CTA whose chunk completes a request (per-request counter) runs
+//    that request's epilogue: accepted length, bonus token, the rebuild
+//    metadata of its verified and MASK slots, and the embedding half of the
+//    rows whose token depends on verification.
+//  * Copy tiles write everything of X that verification cannot change: the
+//    hidden half of every row, the MASK rows' emb(mask) (+) h_shared, and
+//    whole prompt rows (prefill) with their metadata.  The two kinds of
+//    writers touch disjoint bytes, so no ordering between them is needed.
+#include "pe_internal.cuh"
+#include "pe_workspace.cuh"
+
+namespace pe {
+
+struct StepParams {
+  int B, Kp, K, V, H, R, T, mask_id, bt_width, block_size;
+  int full;               // 1: rebuild + assemble too; 0: verification only
+  int nvh;                // 16-byte vectors per half row of X
+  long long row_bytes;    // logits row stride in bytes
+  int nvec, tail;         // whole 16-byte vectors per logits row, leftover elements
+  int chunk_vecs, C, Rl;  // argmax chunking: vectors per chunk, chunks per row, rows
+  int n_arg_units, rows_per_unit, n_copy_units, n_units;
+  const void* logits;
+  const int32_t* in_offsets;
+  const int32_t* in_tokens;
+  const int32_t* in_positions;
+  const int32_t* block_table;
+  const uint4* emb;
+  const uint4* hidden;
+  const uint4* h_shared;
+  int32_t* accepted_len;
+  int32_t* bonus_token;
+  int32_t* target_argmax;
+  int32_t* out_offsets;
+  int32_t* out_tokens;
+  int32_t* out_positions;
+  uint8_t* is_rejected;
+  uint8_t* is_masked;
+  int32_t* hidden_map;
+  long long* slot_mapping;
+  int32_t* sample_idx;
+  uint4* X;
+  uint32_t* sched;
+  uint32_t* count;
+  unsigned long long* keys;
+  uint32_t* err;
+};
+
+enum SegMode { kSkip = 0, kCopy = 1, kZero = 2 };
+
+struct SharedState {
+  unsigned long long red[kWarps];
+  int unit;
+  int last;
+  int first;
+  int amax[PE_MAX_KP + 1];
+  int tok[PE_MAX_KP + 1];
+  const uint4* src[2 * kMaxRowsPerUnit];
+  uint4* dst[2 * kMaxRowsPerUnit];
+  int mode[2 * kMaxRowsPerUnit];
+};
+
+__device__ __forceinline__ int seg_begin(const StepParams& p, int b) {
+  return p.in_offsets ? __ldg(p.in_offsets + b) : b * (p.Kp + 1);
+}
+
+// Segment (request b, its input offset io and length n) of output row t.
+__device__ __forceinline__ void locate(const StepParams& p, int t, int& b, int& io,
+                                       int& n) {
+  if (!p.in_offsets) {
+    b = t / (p.Kp + p.K);
+    io = b * (p.Kp + 1);
+    n = p.Kp + 1;
+    return;
+  }
+  int lo = 0, hi = p.B - 1;  // largest b with oo_b = io_b + b(K-1) <= t
+  while (lo < hi) {
+    int mid = (lo + hi + 1) >> 1;
+    if (__ldg(p.in_offsets + mid) + mid * (p.K - 1) <= t)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  b = lo;
+  io = __ldg(p.in_offsets + b);
+  n = __ldg(p.in_offsets + b + 1) - io;
+}
+
+// ------------------------------------------------------------ element types
+template <int DT>
+struct Elem;
+
+template <>
+struct Elem<PE_BF16> {
+  static constexpr int kPerVec = 8;
+  __device__ static __forceinline__ uint4 neg_inf() {
+    return make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
+  }
+  // max of the 8 elements of a vector (exact: max returns one of its inputs)
+  __device__ static __forceinline__ float vmax(uint4 q) {
+    const uint32_t w = bf16x2_max(bf16x2_max(q.x, q.y), bf16x2_max(q.z, q.w));
+    return fmaxf(bf16_lo(w), bf16_hi(w));
+  }
+  // lowest element of q equal to v (v is known to occur in q)
+  __device__ static __forceinline__ int first_equal(uint4 q, float v) {
+    int e = 7;
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 3; i >= 0; --i) {
+      if (bf16_hi(w[i]) == v) e = 2 * i + 1;
+      if (bf16_lo(w[i]) == v) e = 2 * i;
+    }
+    return e;
+  }
+  __device__ static __forceinline__ float scalar(const char* row, int col) {
+    uint16_t h = __ldg(reinterpret_cast<const unsigned short*>(row) + col);
+    return __uint_as_float(((uint32_t)h) << 16);
+  }
+};
+
+template <>
+struct Elem<PE_F32> {
+  static constexpr int kPerVec = 4;
+  __device__ static __forceinline__ uint4 neg_inf() {
+    return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
+  }
+  __device__ static __forceinline__ float vmax(uint4 q) {
+    return fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)),
+                 fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
+  }
+  __device__ static __forceinline__ int first_equal(uint4 q, float v) {
+    int e = 3;
+    if (__uint_as_float(q.z) == v) e = 2;
+    if (__uint_as_float(q.y) == v) e = 1;
+    if (__uint_as_float(q.x) == v) e = 0;
+    return e;
+  }
+  __device__ static __forceinline__ float scalar(const char* row, int col) {
+    return __ldg(reinterpret_cast<const float*>(row) + col);
+  }
+};
+
+// ------------------------------------------------------------------ epilogue
+// Runs in the CTA that finished the last argmax chunk of request b.
+__device__ void request_epilogue(const StepParams& p, SharedState& sh, int b) {
+  const int tid = threadIdx.x;
+  const int nr = p.Kp + 1;
+  for (int j = tid; j < nr; j += kThreads) {
+    unsigned long long k = atomicExch(p.keys + (long long)b * nr + j, 0ull);
+    int col = (int)key_col(k);
+    sh.amax[j] = col;
+    if (p.target_argmax) p.target_argmax[(long long)b * nr + j] = col;
+  }
+  if (tid == 0) {
+    sh.first = p.Kp;
+    atomicExch(p.count + b, 0u);
+  }
+  __syncthreads();
+
+  const int io = seg_begin(p, b);
+  const int n = seg_begin(p, b + 1) - io;
+  const int vb = n - 1 - p.Kp;  // segment row of the first verified row
+  // accepted length: first draft that differs from the target's choice
+  for (int j = tid; j < p.Kp; j += kThreads)
+    if (sh.amax[j] != __ldg(p.in_tokens + io + vb + j + 1)) atomicMin(&sh.first, j);
+  __syncthreads();
+  const int a = sh.first;
+  const int s = vb + a;  // next-token-prediction slot
+  const int bonus = sh.amax[a];
+  if (!p.full) {
+    if (tid == 0) {
+      p.accepted_len[b] = a;
+      p.bonus_token[b] = bonus;
+    }
+    return;
+  }
+
+  const int oo = io + b * (p.K - 1);
+  if (tid == 0) {
+    p.accepted_len[b] = a;
+    p.bonus_token[b] = bonus;
+    p.out_offsets[b] = oo;
+    if (b == p.B - 1) p.out_offsets[p.B] = p.T;
+  }
+  const int pos_s = __ldg(p.in_positions + io + s);
+  // rebuild metadata of the verified rows (j <= Kp) and MASK rows (j > Kp)
+  for (int j = tid; j < p.Kp + p.K; j += kThreads) {
+    const int k = vb + j;
+    const int t = oo + k;
+    int tok, pos, rej = 0, msk = 0;
+    if (k < s) {
+      tok = __ldg(p.in_tokens + io + k + 1);
+      pos = __ldg(p.in_positions + io + k);
+    } else if (k == s) {
+      tok = bonus;
+      pos = pos_s;
+    } else if (k < n) {
+      rej = 1;
+      tok = (k < n - 1) ? __ldg(p.in_tokens + io + k + 1) : p.mask_id;
+      pos = __ldg(p.in_positions + io + k);
+    } else {
+      msk = 1;
+      tok = p.mask_id;
+      pos = pos_s + (k - n + 1);
+    }
+    p.out_tokens[t] = tok;
+    p.out_positions[t] = pos;
+    p.is_rejected[t] = (uint8_t)rej;
+    p.is_masked[t] = (uint8_t)msk;
+    p.slot_mapping[t] =
+        rej ? -1 : kv_slot(p.block_table, p.bt_width, p.block_size, b, pos, p.err);
+    if (k < n) {
+      p.hidden_map[io + k] = t;
+      sh.tok[j] = tok;
+    }
+    if (p.sample_idx) {
+      if (k == s) p.sample_idx[(long long)b * p.K] = t;
+      if (k >= n) p.sample_idx[(long long)b * p.K + (k - n + 1)] = t;
+    }
+  }
+  __syncthreads();
+
+  // embedding half of the verified rows: emb(token) of the slot's new token
+  const int total = nr * p.nvh;
+  for (int q0 = 0; q0 < total; q0 += kBatchVecs) {
+    uint4 v[kVecPerThread];
+    long long dst[kVecPerThread];
+#pragma unroll
+    for (int i = 0; i < kVecPerThread; ++i) {
+      const int q = q0 + i * kThreads + tid;
+      dst[i] = -1;
+      if (q < total) {
+        const int j = q / p.nvh;
+        const int c = q - j * p.nvh;
+        const int tok = sh.tok[j];
+        dst[i] = (long long)(oo + vb + j) * 2 * p.nvh + c;
+        if (tok >= 0 && tok < p.V) {
+          v[i] = __ldg(p.emb + (long long)tok * p.nvh + c);
+        } else {
+          v[i] = make_uint4(0u, 0u, 0u, 0u);
+          if (c == 0) atomicOr(p.err, PE_ERR_TOKEN_RANGE);
+        }
+      }
+    }
+#pragma unroll
+    for (int i = 0; i < kVecPerThread; ++i)
+      if (dst[i] >= 0) p.X[dst[i]] = v[i];
+  }
+}
+
+// ------------------------------------------------------------- argmax chunk
+template <int DT>
+__device__ void argmax_unit(const StepParams& p, SharedState& sh, int u) {
+  using E = Elem<DT>;
+  const int tid = threadIdx.x;
+  const int r = u / p.C;
+  const int c = u - r * p.C;
+  const char* rowp = static_cast<const char*>(p.logits) + (long long)r * p.row_bytes;
+  const uint4* row = reinterpret_cast<const uint4*>(rowp);
+  const int v_lo = c * p.chunk_vecs;
+  const int v_hi = min(v_lo + p.chunk_vecs, p.nvec);
+
+  // Running maximum of this thread's elements and the column of its first
+  // occurrence.  Elements are visited in increasing column order (batch,
+  // then vector i, then element), so a strict '>' keeps the first one.
+  float m = 0.f;
+  int col = -1;
+  for (int base = v_lo; base < v_hi; base += kBatchVecs) {
+    if (base + tid >= v_hi) break;  // this thread has no vector here or later
+    uint4 x[kVecPerThread];
+#pragma unroll
+    for (int i = 0; i < kVecPerThread; ++i) {
+      const int v = base + i * kThreads + tid;
+      x[i] = v < v_hi ? __ldcs(row + v) : E::neg_inf();
+    }
+    float vm[kVecPerThread];
+#pragma unroll
+    for (int i = 0; i < kVecPerThread; ++i) vm[i] = E::vmax(x[i]);
+    float gm = vm[0];
+#pragma unroll
+    for (int i = 1; i < kVecPerThread; ++i) gm = fmaxf(gm, vm[i]);
+    if (col < 0 || gm > m) {
+      // locate the first vector, then the first element, holding gm
+      uint4 q = x[kVecPerThread - 1];
+      int vi = kVecPerThread - 1;
+#pragma unroll
+      for (int i = kVecPerThread - 2; i >= 0; --i)
+        if (vm[i] == gm) {
+          q = x[i];
+          vi = i;
+        }
+      m = gm;
+      col = (base + vi * kThreads + tid) * E::kPerVec + E::first_equal(q, gm);
+    }
+  }
+  unsigned long long key = col >= 0 ? make_key(m, (uint32_t)col) : 0ull;
+
+  // leftover elements past the last whole vector (last chunk, one thread)
+  if (p.tail && c == p.C - 1 && tid == 0) {
+    const int c0 = p.nvec * E::kPerVec;
+    float tm = E::scalar(rowp, c0);
+    int tc = c0;
+    for (int e = 1; e < p.tail; ++e) {
+      const float x = E::scalar(rowp, c0 + e);
+      if (x > tm) {
+        tm = x;
+        tc = c0 + e;
+      }
+    }
+    const unsigned long long tk = make_key(tm, (uint32_t)tc);
+    key = tk > key ? tk : key;
+  }
+
+  key = warp_max_key(key);
+  if ((tid & 31) == 0) sh.red[tid >> 5] = key;
+  __syncthreads();
+  if (tid < 32) {
+    unsigned long long k = tid < kWarps ? sh.red[tid] : 0ull;
+    k = warp_max_key(k);
+    if (tid == 0) {
+      atomicMax(p.keys + r, k);
+      __threadfence();
+      const int b = r / (p.Kp + 1);
+      const unsigned done = atomicAdd(p.count + b, 1u);
+      sh.last = (done == (unsigned)((p.Kp + 1) * p.C - 1)) ? b : -1;
+    }
+  }
+  __syncthreads();
+  const int last = sh.last;
+  if (last >= 0) {
+    __threadfence();
+    request_epilogue(p, sh, last);
+  }
+}
+
+// ------------------------------------------------------------------ X tiles
+// Rows whose content verification cannot change: hidden half of every row,
+// MASK rows entirely, prompt rows (prefill) entirely plus their metadata.
+__device__ void copy_unit(const StepParams& p, SharedState& sh, int u) {
+  const int tid = threadIdx.x;
+  const int t0 = u * p.rows_per_unit;
+  const int nrows = min(p.rows_per_unit, p.T - t0);
+  if (tid < nrows) {
+    const int t = t0 + tid;
+    int b, io, n;
+    locate(p, t, b, io, n);
+    const int oo = io + b * (p.K - 1);
+    const int k = t - oo;
+    const int vb = n - 1 - p.Kp;
+    uint4* xr = p.X + (long long)t * 2 * p.nvh;
+    int me;
+    const uint4* se = nullptr;
+    const uint4* sh_src;
+    if (k < vb) {  // prompt row: shifted token, own hidden row
+      const int tok = __ldg(p.in_tokens + io + k + 1);
+      const int pos = __ldg(p.in_positions + io + k);
+      p.out_tokens[t] = tok;
+      p.out_positions[t] = pos;
+      p.is_rejected[t] = 0;
+      p.is_masked[t] = 0;
+      p.slot_mapping[t] = kv_slot(p.block_table, p.bt_width, p.block_size, b, pos, p.err);
+      p.hidden_map[io + k] = t;
+      if (tok >= 0 && tok < p.V) {
+        me = kCopy;
+        se = p.emb + (long long)tok * p.nvh;
+      } else {
+        me = kZero;
+        atomicOr(p.err, PE_ERR_TOKEN_RANGE);
+      }
+      sh_src = p.hidden + (long long)(io + k) * p.nvh;
+    } else if (k < n) {  // verified row: its embedding half waits for the bonus
+      me = kSkip;
+      sh_src = p.hidden + (long long)(io + k) * p.nvh;
+    } else {  // MASK row: emb(mask) (+) h_shared
+      me = kCopy;
+      se = p.emb + (long long)p.mask_id * p.nvh;
+      sh_src = p.h_shared;
+    }
+    sh.mode[2 * tid] = me;
+    sh.src[2 * tid] = se;
+    sh.dst[2 * tid] = xr;
+    sh.mode[2 * tid + 1] = kCopy;
+    sh.src[2 * tid + 1] = sh_src;
+    sh.dst[2 * tid + 1] = xr + p.nvh;
+  }
+  __syncthreads();
+  const int nseg = 2 * nrows;
+  constexpr int kSeg = 4;   // half rows per batch
+  constexpr int kCols = 2;  // vectors per thread per half row per batch
+  for (int v0 = 0; v0 < p.nvh; v0 += kCols * kThreads) {
+    for (int sg = 0; sg < nseg; sg += kSeg) {
+      uint4 buf[kSeg][kCols];
+#pragma unroll
+      for (int s = 0; s < kSeg; ++s) {
+        const int md = (sg + s < nseg) ? sh.mode[sg + s] : kSkip;
+        const uint4* src = (sg + s < nseg) ? sh.src[sg + s] : nullptr;
+#pragma unroll
+        for (int i = 0; i < kCols; ++i) {
+          const int v = v0 + i * kThreads + tid;
+          if (md == kCopy && v < p.nvh)
+            buf[s][i] = __ldg(src + v);
+          else
+            buf[s][i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+#pragma unroll
+      for (int s = 0; s < kSeg; ++s) {
+        const int md = (sg + s < nseg) ? sh.mode[sg + s] : kSkip;
+        uint4* dst = (sg + s < nseg) ? sh.dst[sg + s] : nullptr;
+#pragma unroll
+        for (int i = 0; i < kCols; ++i) {
+          const int v = v0 + i * kThreads + tid;
+          if (md != kSkip && v < p.nvh) dst[v] = buf[s][i];
+        }
+      }
+    }
+  }
+}
+
+// ------------------------------------------------------------------- kernel
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 3) step_kernel(const StepParams p) {
+  __shared__ SharedState sh;
+  if (p.in_offsets && !offsets_valid(p.in_offsets, p.B, p.R, p.Kp + 1)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.err, PE_ERR_OFFSETS);
+    return;  // every CTA sees the same offsets and leaves without writing
+  }
+  if (threadIdx.x == 0) sh.unit = (int)atomicAdd(p.sched, 1u);
+  __syncthreads();
+  int u = sh.unit;
+  while (u < p.n_units) {
+    unsigned next = 0;
+    if (threadIdx.x == 0) next = atomicAdd(p.sched, 1u);  // prefetch the next unit
+    if (u < p.n_arg_units)
+      argmax_unit<DT>(p, sh, u);
+    else
+      copy_unit(p, sh, u - p.n_arg_units);
+    __syncthreads();
+    if (threadIdx.x == 0) sh.unit = (int)next;
+    __syncthreads();
+    u = sh.unit;
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned done = atomicAdd(p.sched + 1, 1u);
+    if (done == gridDim.x - 1) {  // every CTA has taken its last unit
+      atomicExch(p.sched, 0u);
+      atomicExch(p.sched + 1, 0u);
+    }
+  }
+}
+
+}  // namespace pe
+
+// ---------------------------------------------------------------- host side
+namespace {
+
+using pe_host::aligned16;
+using pe_host::elt_size;
+
+// Argmax chunking and grid size for `rows` logits rows of `V` elements.
+void plan_argmax(pe::StepParams& p, int elt, int rows, int grid_max, int batches) {
+  const int epv = 16 / elt;
+  p.Rl = rows;
+  p.nvec = p.V / epv;
+  p.tail = p.V % epv;
+  if (p.nvec == 0) {
+    p.C = 1;
+    p.chunk_vecs = 0;
+  } else {
+    const long long cap = (long long)batches * pe::kBatchVecs;
+    int c_min = (int)((p.nvec + cap - 1) / cap);
+    int c_want = (grid_max + rows - 1) / rows;  // at least ~one unit per CTA
+    int c_max = (p.nvec + pe::kThreads - 1) / pe::kThreads;
+    int C = c_min > c_want ? c_min : c_want;
+    if (C > c_max) C = c_max;
+    if (C < 1) C = 1;
+    int chunk = (p.nvec + C - 1) / C;
+    if (chunk > pe::kBatchVecs)  // whole batches, so only a row's last chunk is ragged
+      chunk = (chunk + pe::kBatchVecs - 1) / pe::kBatchVecs * pe::kBatchVecs;
+    p.chunk_vecs = chunk;
+    p.C = (p.nvec + chunk - 1) / chunk;
+  }
+  p.n_arg_units = rows * p.C;
+}
+
+int launch(const pe::StepParams& p, int dtype, int grid, cudaStream_t stream) {
+  if (dtype == PE_BF16)
+    pe::step_kernel<PE_BF16><<<grid, pe::kThreads, 0, stream>>>(p);
+  else
+    pe::step_kernel<PE_F32><<<grid, pe::kThreads, 0, stream>>>(p);
+  return pe_host::launch_status();
+}
+
+void bind_workspace(pe::StepParams& p, void* ws, int rows, int B) {
+  pe::WorkspaceLayout L(rows, B);
+  char* base = static_cast<char*>(ws);
+  p.sched = reinterpret_cast<uint32_t*>(base);
+  p.count = reinterpret_cast<uint32_t*>(base + L.count_off);
+  p.keys = reinterpret_cast<unsigned long long*>(base + L.key_off);
+}
+
+}  // namespace
+
+extern "C" {
+
+int pe_verify_greedy(const void* logits, int dtype, int64_t row_stride, int32_t B,
+                     int32_t Kp, int32_t V, const int32_t* in_tokens,
+                     int32_t* accepted_len, int32_t* bonus_token,
+                     int32_t* target_argmax, void* workspace, uint32_t* err,
+                     void* stream) {
+  const int elt = elt_size(dtype);
+  if (!elt) return PE_EDTYPE;
+  if (B < 0 || Kp < 0 || Kp > PE_MAX_KP || V < 1) return PE_EINVAL;
+  if (B == 0) return PE_OK;
+  if ((long long)B * (Kp + 1) > 0x7fffffffLL || row_stride < V) return PE_EINVAL;
+  if (!logits || !accepted_len || !bonus_token || !workspace || !err) return PE_EINVAL;
+  if (Kp > 0 && !in_tokens) return PE_EINVAL;
+  if (!aligned16(logits) || !aligned16(workspace) || (row_stride * elt) % 16)
+    return PE_EALIGN;
+  pe_host::DeviceInfo dev;
+  if (pe_host::device_info(&dev) != PE_OK) return PE_ECUDA;
+  const pe_host::Tuning tn = pe_host::tuning();
+
+  pe::StepParams p = {};
+  p.B = B;
+  p.Kp = Kp;
+  p.K = 1;
+  p.V = V;
+  p.full = 0;
+  p.row_bytes = row_stride * elt;
+  p.logits = logits;
+  p.in_tokens = in_tokens;
+  p.accepted_len = accepted_len;
+  p.bonus_token = bonus_token;
+  p.target_argmax = target_argmax;
+  p.err = err;
+  const int rows = B * (Kp + 1);
+  const int grid_max = dev.sm_count * tn.ctas_per_sm;
+  plan_argmax(p, elt, rows, grid_max, tn.chunk_batches);
+  p.n_units = p.n_arg_units;
+  bind_workspace(p, workspace, rows, B);
+  const int grid = p.n_units < grid_max ? p.n_units : grid_max;
+  return launch(p, dtype, grid, static_cast<cudaStream_t>(stream));
+}
+
+int pe_step(const pe_step_args* a, void* stream) {
+  if (!a) return PE_EINVAL;
+  const int elt = elt_size(a->logits_dtype);
+  const int xelt = elt_size(a->x_dtype);
+  if (!elt || !xelt) return PE_EDTYPE;
+  const int B = a->B, Kp = a->Kp, K = a->K;
+  if (B < 0 || Kp < 0 || Kp > PE_MAX_KP || K < 1 || K > PE_MAX_K) return PE_EINVAL;
+  if (a->V < 1 || a->H < 1 || a->mask_id < 0 || a->mask_id >= a->V) return PE_EINVAL;
+  if (a->bt_width < 1 || a->block_size < 1 || a->logits_row_stride < a->V)
+    return PE_EINVAL;
+  if (B == 0) {
+    if (!a->out_offsets) return PE_EINVAL;
+    return cudaMemsetAsync(a->out_offsets, 0, sizeof(int32_t),
+                           static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? PE_OK
+               : PE_ECUDA;
+  }
+  if (Kp >= 1) {
+    if (a->in_offsets || (long long)a->R != (long long)B * (Kp + 1)) return PE_EINVAL;
+  } else {
+    if (!a->in_offsets || a->R < B) return PE_EINVAL;
+  }
+  const long long T = (long long)a->R + (long long)B * (K - 1);
+  if ((long long)B * (Kp + 1) > 0x7fffffffLL || T > 0x7fffffffLL) return PE_EINVAL;
+  if (!a->logits || !a->in_tokens || !a->in_positions || !a->block_table || !a->emb ||
+      !a->target_hidden || !a->h_shared || !a->accepted_len || !a->bonus_token ||
+      !a->out_offsets || !a->out_tokens || !a->out_positions || !a->is_rejected ||
+      !a->is_masked || !a->hidden_map || !a->slot_mapping || !a->X || !a->workspace ||
+      !a->err)
+    return PE_EINVAL;
+  if (!aligned16(a->logits) || !aligned16(a->emb) || !aligned16(a->target_hidden) ||
+      !aligned16(a->h_shared) || !aligned16(a->X) || !aligned16(a->workspace) ||
+      (a->logits_row_stride * elt) % 16 || ((long long)a->H * xelt) % 16)
+    return PE_EALIGN;
+  pe_host::DeviceInfo dev;
+  if (pe_host::device_info(&dev) != PE_OK) return PE_ECUDA;
+  const pe_host::Tuning tn = pe_host::tuning();
+
+  pe::StepParams p = {};
+  p.B = B;
+  p.Kp = Kp;
+  p.K = K;
+  p.V = a->V;
+  p.H = a->H;
+  p.R = a->R;
+  p.T = (int)T;
+  p.mask_id = a->mask_id;
+  p.bt_width = a->bt_width;
+  p.block_size = a->block_size;
+  p.full = 1;
+  p.nvh = (int)((long long)a->H * xelt / 16);
+  p.row_bytes = a->logits_row_stride * elt;
+  p.logits = a->logits;
+  p.in_offsets = a->in_offsets;
+  p.in_tokens = a->in_tokens;
+  p.in_positions = a->in_positions;
+  p.block_table = a->block_table;
+  p.emb = static_cast<const uint4*>(a->emb);
+  p.hidden = static_cast<const uint4*>(a->target_hidden);
+  p.h_shared = static_cast<const uint4*>(a->h_shared);
+  p.accepted_len = a->accepted_len;
+  p.bonus_token = a->bonus_token;
+  p.target_argmax = a->target_argmax;
+  p.out_offsets = a->out_offsets;
+  p.out_tokens = a->out_tokens;
+  p.out_positions = a->out_positions;
+  p.is_rejected = a->is_rejected;
+  p.is_masked = a->is_masked;
+  p.hidden_map = a->hidden_map;
+  p.slot_mapping = reinterpret_cast<long long*>(a->slot_mapping);
+  p.sample_idx = a->sample_idx;
+  p.X = static_cast<uint4*>(a->X);
+  p.err = a->err;
+  const int rows = B * (Kp + 1);
+  const int grid_max = dev.sm_count * tn.ctas_per_sm;
+  plan_argmax(p, elt, rows, grid_max, tn.chunk_batches);
+  p.rows_per_unit = tn.rows_per_unit;
+  p.n_copy_units = (p.T + p.rows_per_unit - 1) / p.rows_per_unit;
+  p.n_units = p.n_arg_units + p.n_copy_units;
+  bind_workspace(p, a->workspace, rows, B);
+  const int grid = p.n_units < grid_max ? p.n_units : grid_max;
+  return launch(p, a->logits_dtype, grid, static_cast<cudaStream_t>(stream));
+}
+
+}  // extern "C"
