@@ -85,6 +85,13 @@ def sum_over_ranks(x: float, world: int, device) -> float:
     return float(t.item())
 
 
+def aggregate(rows_this_rank: float, ms_this_rank: float, world: int, device):
+    """Whole-job throughput: rows of all ranks over the slowest rank's time."""
+    ms = max_over_ranks(ms_this_rank, world, device)
+    rows = sum_over_ranks(rows_this_rank, world, device)
+    return rows / (ms / 1e3), ms, rows
+
+
 def rank_seed(workload: str, rank: int) -> int:
     """Each rank draws its own independent requests."""
     return 5000 + 97 * (list(wl.SPECS).index(workload) + 1) + rank
@@ -166,10 +173,6 @@ class ClockSampler:
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
-        self.windows = []
-
-    def mark(self):
-        return time.time()
 
     def stop(self, t0: float, t1: float) -> dict:
         if self.proc is None:
@@ -347,11 +350,8 @@ def run_ours(args):
     clocks = sampler.stop(t_wall0, t_wall1)
     step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     mean_ms = sum(step_ms) / len(step_ms)
-    mean_ms_max = max_over_ranks(mean_ms, world, device)
-
     T = w.T
-    rows_all = sum_over_ranks(float(T), world, device)
-    value = rows_all / (mean_ms_max / 1e3)
+    value, mean_ms_max, rows_all = aggregate(float(T), mean_ms, world, device)
 
     bytes_ = algorithmic_bytes(spec, w.R)
     peak, peak_kind = measured_peak()

@@ -298,7 +298,7 @@ def test_workspace_reused_across_calls_and_sizes():
     ws = _native.new_workspace(256 * 8, 256)   # sized for the largest batch
     for i, spec in enumerate([wl.SPECS["decode_b256"].with_(B=256, V=30011, row_pad=5),
                               wl.SPECS["tiny"], wl.SPECS["decode_b256"].with_(B=17),
-                              wl.SPECS["prefill_b8"].with_(B=5, prompt_hi=700, H=64),
+                              wl.SPECS["prefill_b8"].with_(B=5, prompt_lo=1, prompt_hi=700, H=64),
                               wl.SPECS["decode_b256"].with_(B=256, V=30011, row_pad=5)]):
         w = _gen(spec, 100 + i)
         assert_same(run_fused(w, workspace=ws), oracle_of(w), what="call %d" % i)
