@@ -195,6 +195,28 @@ typedef struct pe_step_args {
 
 int pe_step(const pe_step_args* args /* host */, void* stream);
 
+/* pe_step for callers that cannot allocate device memory at all, not even
+ * the small scratch above: code running under a memory manager that owns
+ * the whole device, plug-ins that only receive the tensors they work on,
+ * loops that must not hit the device-wide synchronisation of cudaMalloc /
+ * cudaFree.  The pages have no counterpart of this entry point.
+ * Outputs are identical to pe_step's; args->workspace is ignored (may be
+ * NULL).  The scratch is a fixed array of PE_NOALLOC_WS_BYTES bytes inside
+ * the library, held by every GPU that loads it until the process exits.
+ *  - The first call on a device looks up the array's device address (and
+ *    may load the library's GPU code there): make that first call before
+ *    any stream capture.
+ *  - Each call enqueues a memset clearing the scratch it needs, then the
+ *    step; if pe_step then rejects the arguments, the memset has still been
+ *    enqueued (it touches only the library's own array).
+ *  - A batch that needs more than PE_NOALLOC_WS_BYTES of scratch
+ *    (pe_workspace_bytes(B*(Kp+1), B)) is rejected with PE_EINVAL.
+ *  - Every call shares the array: calls whose work overlaps on the GPU
+ *    race on it, so order them (one stream, or events between streams).
+ *  - Nothing is allocated or freed. */
+#define PE_NOALLOC_WS_BYTES 65536
+int pe_step_noalloc(const pe_step_args* args /* host */, void* stream);
+
 /* Launch-shape knobs of the fused step (process-wide; defaults chosen by
  * measurement).  Zero fields keep the current value. */
 typedef struct pe_tuning {

@@ -28,8 +28,8 @@ MAX_KP, MAX_K = 255, 256
 
 # every function the C header declares
 EXPORTS = ("pe_workspace_bytes", "pe_verify_greedy", "pe_build_draft_batch",
-           "pe_assemble_draft_inputs", "pe_step", "pe_get_tuning", "pe_set_tuning",
-           "pe_status_str")
+           "pe_assemble_draft_inputs", "pe_step", "pe_step_noalloc", "pe_get_tuning",
+           "pe_set_tuning", "pe_status_str")
 
 
 class PEError(RuntimeError):
@@ -90,6 +90,8 @@ def load():
                                               i32, i32] + [P] * 10)
         lib.pe_assemble_draft_inputs.argtypes = [ctypes.c_int, i32, i32, i32, i32] + [P] * 9
         lib.pe_step.argtypes = [ctypes.POINTER(StepArgs), P]
+        lib.pe_step_noalloc.argtypes = [ctypes.POINTER(StepArgs), P]
+        lib.pe_step_noalloc.restype = ctypes.c_int
         lib.pe_get_tuning.argtypes = [ctypes.POINTER(Tuning)]
         lib.pe_set_tuning.argtypes = [ctypes.POINTER(Tuning)]
         lib.pe_status_str.argtypes = [ctypes.c_int]
