@@ -164,7 +164,8 @@ struct Elem<PE_F32> {
 
 // ------------------------------------------------------------------ epilogue
 // Runs in the CTA that finished the last argmax chunk of request b.
-__device__ void request_epilogue(const StepParams& p, SharedState& sh, int b) {
+__device__ __forceinline__ void request_epilogue(const StepParams& p, SharedState& sh,
+                                                 int b) {
   const int tid = threadIdx.x;
   const int nr = p.Kp + 1;
   for (int j = tid; j < nr; j += kThreads) {
@@ -272,7 +273,7 @@ __device__ void request_epilogue(const StepParams& p, SharedState& sh, int b) {
 
 // ------------------------------------------------------------- argmax chunk
 template <int DT>
-__device__ void argmax_unit(const StepParams& p, SharedState& sh, int u) {
+__device__ __forceinline__ void argmax_unit(const StepParams& p, SharedState& sh, int u) {
   using E = Elem<DT>;
   const int tid = threadIdx.x;
   const int r = u / p.C;
@@ -358,7 +359,7 @@ __device__ void argmax_unit(const StepParams& p, SharedState& sh, int u) {
 // ------------------------------------------------------------------ X tiles
 // Rows whose content verification cannot change: hidden half of every row,
 // MASK rows entirely, prompt rows (prefill) entirely plus their metadata.
-__device__ void copy_unit(const StepParams& p, SharedState& sh, int u) {
+__device__ __forceinline__ void copy_unit(const StepParams& p, SharedState& sh, int u) {
   const int tid = threadIdx.x;
   const int t0 = u * p.rows_per_unit;
   const int nrows = min(p.rows_per_unit, p.T - t0);
@@ -447,12 +448,12 @@ __global__ void __launch_bounds__(kThreads, 3) step_kernel(const StepParams p) {
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.err, PE_ERR_OFFSETS);
     return;  // every CTA sees the same offsets and leaves without writing
   }
-  if (threadIdx.x == 0) sh.unit = (int)atomicAdd(p.sched, 1u);
-  __syncthreads();
-  int u = sh.unit;
+  // The first unit of each CTA is its own index; later units come from the
+  // counter, which therefore hands out gridDim.x + 0, 1, 2, ...
+  int u = blockIdx.x;
   while (u < p.n_units) {
     unsigned next = 0;
-    if (threadIdx.x == 0) next = atomicAdd(p.sched, 1u);  // prefetch the next unit
+    if (threadIdx.x == 0) next = gridDim.x + atomicAdd(p.sched, 1u);  // prefetch
     if (u < p.n_arg_units)
       argmax_unit<DT>(p, sh, u);
     else
