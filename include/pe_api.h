@@ -66,6 +66,8 @@ typedef enum pe_dtype { PE_F32 = 0, PE_BF16 = 1 } pe_dtype;
 #define PE_ERR_SLOT_RANGE 4u  /* accepted_len outside [0,Kp]: taken as 0    */
 #define PE_ERR_OFFSETS 8u     /* in_offsets invalid: nothing is written     */
 #define PE_ERR_MAP_RANGE 16u  /* hidden_map entry outside [0,T): skipped    */
+#define PE_ERR_TIMEOUT 32u    /* a bounded pipeline wait gave up (outputs
+                                 incomplete; never expected)               */
 
 /* Limits checked on the host. */
 #define PE_MAX_KP 255 /* previous draft depth K'  */
@@ -223,6 +225,7 @@ typedef struct pe_tuning {
   int32_t ctas_per_sm;     /* resident CTAs per SM for the persistent grid */
   int32_t chunk_batches;   /* max 32 KiB load batches per argmax unit      */
   int32_t rows_per_unit;   /* X rows per copy unit                         */
+  int32_t variant;         /* 1: register streaming, 2: bulk-copy pipeline */
 } pe_tuning;
 int pe_get_tuning(pe_tuning* out /* host */);
 int pe_set_tuning(const pe_tuning* in /* host */);

@@ -24,6 +24,7 @@ ERR_BLOCK_RANGE = 2
 ERR_SLOT_RANGE = 4
 ERR_OFFSETS = 8
 ERR_MAP_RANGE = 16
+ERR_TIMEOUT = 32
 MAX_KP, MAX_K = 255, 256
 
 # every function the C header declares
@@ -60,7 +61,8 @@ class StepArgs(ctypes.Structure):
 
 class Tuning(ctypes.Structure):
     """Mirror of pe_tuning."""
-    _fields_ = [("ctas_per_sm", i32), ("chunk_batches", i32), ("rows_per_unit", i32)]
+    _fields_ = [("ctas_per_sm", i32), ("chunk_batches", i32), ("rows_per_unit", i32),
+                ("variant", i32)]
 
 
 _lock = threading.Lock()

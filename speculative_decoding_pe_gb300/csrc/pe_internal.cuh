@@ -97,6 +97,7 @@ struct Tuning {
   int ctas_per_sm;
   int chunk_batches;
   int rows_per_unit;
+  int variant;
 };
 Tuning tuning();
 

@@ -30,9 +30,19 @@
 //    whole prompt rows (prefill) with their metadata.  The two kinds of
 //    writers touch disjoint bytes, so no ordering between them is needed.
 #include "pe_internal.cuh"
+#include "pe_tma.cuh"
 #include "pe_workspace.cuh"
 
 namespace pe {
+
+// Barrier over the threads that do a unit's work: the whole CTA in the
+// register-streaming kernel, the eight consumer warps in the pipelined one.
+struct SyncAll {
+  __device__ static __forceinline__ void sync() { __syncthreads(); }
+};
+struct SyncConsumers {
+  __device__ static __forceinline__ void sync() { named_sync<kThreads>(); }
+};
 
 struct StepParams {
   int B, Kp, K, V, H, R, T, mask_id, bt_width, block_size;
@@ -75,8 +85,10 @@ struct SharedState {
   int unit;
   int last;
   int first;
+  int verdict[2];
   int amax[PE_MAX_KP + 1];
   int tok[PE_MAX_KP + 1];
+  int pos[PE_MAX_KP + 1];
   const uint4* src[2 * kMaxRowsPerUnit];
   uint4* dst[2 * kMaxRowsPerUnit];
   int mode[2 * kMaxRowsPerUnit];
@@ -163,32 +175,37 @@ struct Elem<PE_F32> {
 };
 
 // ------------------------------------------------------------------ epilogue
-// Runs in the CTA that finished the last argmax chunk of request b.
+// Runs in the CTA that finished the last argmax chunk of request b.  Its
+// global traffic is two dependent round trips: (1) the row keys (exchanged
+// with 0, leaving the workspace clean), the drafts and the positions of the
+// verified rows, all at once; (2) after the verdict, the embedding rows of
+// the verified slots with their final tokens and the block-table entries of
+// the kept slots.
+template <class S>
 __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedState& sh,
                                                  int b) {
   const int tid = threadIdx.x;
-  const int nr = p.Kp + 1;
-  for (int j = tid; j < nr; j += kThreads) {
-    unsigned long long k = atomicExch(p.keys + (long long)b * nr + j, 0ull);
-    int col = (int)key_col(k);
-    sh.amax[j] = col;
-    if (p.target_argmax) p.target_argmax[(long long)b * nr + j] = col;
-  }
-  if (tid == 0) {
-    sh.first = p.Kp;
-    atomicExch(p.count + b, 0u);
-  }
-  __syncthreads();
-
+  const int Kp = p.Kp;
+  const int nr = Kp + 1;  // verified rows (<= 256 = threads)
   const int io = seg_begin(p, b);
   const int n = seg_begin(p, b + 1) - io;
-  const int vb = n - 1 - p.Kp;  // segment row of the first verified row
+  const int vb = n - 1 - Kp;  // segment row of the first verified row
+  if (tid < nr) {
+    const unsigned long long k = atomicExch(p.keys + (long long)b * nr + tid, 0ull);
+    sh.amax[tid] = (int)key_col(k);
+    if (tid < Kp) sh.tok[tid] = __ldg(p.in_tokens + io + vb + tid + 1);  // draft d_{tid+1}
+    if (p.full) sh.pos[tid] = __ldg(p.in_positions + io + vb + tid);
+  }
+  if (tid == 0) {
+    sh.first = Kp;
+    atomicExch(p.count + b, 0u);
+  }
+  S::sync();
   // accepted length: first draft that differs from the target's choice
-  for (int j = tid; j < p.Kp; j += kThreads)
-    if (sh.amax[j] != __ldg(p.in_tokens + io + vb + j + 1)) atomicMin(&sh.first, j);
-  __syncthreads();
+  if (tid < Kp && sh.amax[tid] != sh.tok[tid]) atomicMin(&sh.first, tid);
+  if (p.target_argmax && tid < nr) p.target_argmax[(long long)b * nr + tid] = sh.amax[tid];
+  S::sync();
   const int a = sh.first;
-  const int s = vb + a;  // next-token-prediction slot
   const int bonus = sh.amax[a];
   if (!p.full) {
     if (tid == 0) {
@@ -197,53 +214,20 @@ __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedStat
     }
     return;
   }
-
   const int oo = io + b * (p.K - 1);
+  const int s = vb + a;        // next-token-prediction slot
+  const int pos_s = sh.pos[a];
   if (tid == 0) {
     p.accepted_len[b] = a;
     p.bonus_token[b] = bonus;
     p.out_offsets[b] = oo;
     if (b == p.B - 1) p.out_offsets[p.B] = p.T;
   }
-  const int pos_s = __ldg(p.in_positions + io + s);
-  // rebuild metadata of the verified rows (j <= Kp) and MASK rows (j > Kp)
-  for (int j = tid; j < p.Kp + p.K; j += kThreads) {
-    const int k = vb + j;
-    const int t = oo + k;
-    int tok, pos, rej = 0, msk = 0;
-    if (k < s) {
-      tok = __ldg(p.in_tokens + io + k + 1);
-      pos = __ldg(p.in_positions + io + k);
-    } else if (k == s) {
-      tok = bonus;
-      pos = pos_s;
-    } else if (k < n) {
-      rej = 1;
-      tok = (k < n - 1) ? __ldg(p.in_tokens + io + k + 1) : p.mask_id;
-      pos = __ldg(p.in_positions + io + k);
-    } else {
-      msk = 1;
-      tok = p.mask_id;
-      pos = pos_s + (k - n + 1);
-    }
-    p.out_tokens[t] = tok;
-    p.out_positions[t] = pos;
-    p.is_rejected[t] = (uint8_t)rej;
-    p.is_masked[t] = (uint8_t)msk;
-    p.slot_mapping[t] =
-        rej ? -1 : kv_slot(p.block_table, p.bt_width, p.block_size, b, pos, p.err);
-    if (k < n) {
-      p.hidden_map[io + k] = t;
-      sh.tok[j] = tok;
-    }
-    if (p.sample_idx) {
-      if (k == s) p.sample_idx[(long long)b * p.K] = t;
-      if (k >= n) p.sample_idx[(long long)b * p.K + (k - n + 1)] = t;
-    }
-  }
-  __syncthreads();
-
-  // embedding half of the verified rows: emb(token) of the slot's new token
+  // Token of verified slot j (segment row vb + j): the bonus at j == a, the
+  // shifted draft d_{j+1} elsewhere, and the MASK id in the last row when it
+  // is rejected.
+  auto slot_token = [&](int j) { return j == a ? bonus : (j < Kp ? sh.tok[j] : p.mask_id); };
+  // embedding half of the verified rows
   const int total = nr * p.nvh;
   for (int q0 = 0; q0 < total; q0 += kBatchVecs) {
     uint4 v[kVecPerThread];
@@ -255,7 +239,7 @@ __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedStat
       if (q < total) {
         const int j = q / p.nvh;
         const int c = q - j * p.nvh;
-        const int tok = sh.tok[j];
+        const int tok = slot_token(j);
         dst[i] = (long long)(oo + vb + j) * 2 * p.nvh + c;
         if (tok >= 0 && tok < p.V) {
           v[i] = __ldg(p.emb + (long long)tok * p.nvh + c);
@@ -269,9 +253,39 @@ __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedStat
     for (int i = 0; i < kVecPerThread; ++i)
       if (dst[i] >= 0) p.X[dst[i]] = v[i];
   }
+  // rebuild metadata of the verified rows (j <= Kp) and MASK rows (j > Kp)
+  for (int j = tid; j < Kp + p.K; j += kThreads) {
+    const int k = vb + j;
+    const int t = oo + k;
+    int tok, pos, rej = 0, msk = 0;
+    if (j <= Kp) {
+      tok = slot_token(j);
+      pos = sh.pos[j];
+      rej = j > a;
+    } else {
+      msk = 1;
+      tok = p.mask_id;
+      pos = pos_s + (j - Kp);
+    }
+    p.out_tokens[t] = tok;
+    p.out_positions[t] = pos;
+    p.is_rejected[t] = (uint8_t)rej;
+    p.is_masked[t] = (uint8_t)msk;
+    p.slot_mapping[t] =
+        rej ? -1 : kv_slot(p.block_table, p.bt_width, p.block_size, b, pos, p.err);
+    if (j <= Kp) p.hidden_map[io + k] = t;
+    if (p.sample_idx) {
+      if (k == s) p.sample_idx[(long long)b * p.K] = t;
+      if (j > Kp) p.sample_idx[(long long)b * p.K + (j - Kp)] = t;
+    }
+  }
 }
 
 // ------------------------------------------------------------- argmax chunk
+template <class S, int DT>
+__device__ __forceinline__ void finish_argmax_unit(const StepParams& p, SharedState& sh, int r,
+                                                   int c, unsigned long long key);
+
 template <int DT>
 __device__ __forceinline__ void argmax_unit(const StepParams& p, SharedState& sh, int u) {
   using E = Elem<DT>;
@@ -316,8 +330,19 @@ __device__ __forceinline__ void argmax_unit(const StepParams& p, SharedState& sh
       col = (base + vi * kThreads + tid) * E::kPerVec + E::first_equal(q, gm);
     }
   }
-  unsigned long long key = col >= 0 ? make_key(m, (uint32_t)col) : 0ull;
+  const unsigned long long key = col >= 0 ? make_key(m, (uint32_t)col) : 0ull;
+  finish_argmax_unit<SyncAll, DT>(p, sh, r, c, key);
+}
 
+// End of an argmax unit: fold in the leftover elements, reduce the threads'
+// keys, merge into the row's key, and run the request's epilogue in the CTA
+// whose unit completes the request.
+template <class S, int DT>
+__device__ __forceinline__ void finish_argmax_unit(const StepParams& p, SharedState& sh, int r,
+                                                   int c, unsigned long long key) {
+  using E = Elem<DT>;
+  const int tid = threadIdx.x;
+  const char* rowp = static_cast<const char*>(p.logits) + (long long)r * p.row_bytes;
   // leftover elements past the last whole vector (last chunk, one thread)
   if (p.tail && c == p.C - 1 && tid == 0) {
     const int c0 = p.nvec * E::kPerVec;
@@ -336,7 +361,7 @@ __device__ __forceinline__ void argmax_unit(const StepParams& p, SharedState& sh
 
   key = warp_max_key(key);
   if ((tid & 31) == 0) sh.red[tid >> 5] = key;
-  __syncthreads();
+  S::sync();
   if (tid < 32) {
     unsigned long long k = tid < kWarps ? sh.red[tid] : 0ull;
     k = warp_max_key(k);
@@ -348,17 +373,18 @@ __device__ __forceinline__ void argmax_unit(const StepParams& p, SharedState& sh
       sh.last = (done == (unsigned)((p.Kp + 1) * p.C - 1)) ? b : -1;
     }
   }
-  __syncthreads();
+  S::sync();
   const int last = sh.last;
   if (last >= 0) {
     __threadfence();
-    request_epilogue(p, sh, last);
+    request_epilogue<S>(p, sh, last);
   }
 }
 
 // ------------------------------------------------------------------ X tiles
 // Rows whose content verification cannot change: hidden half of every row,
 // MASK rows entirely, prompt rows (prefill) entirely plus their metadata.
+template <class S, int kSeg, int kCols>
 __device__ __forceinline__ void copy_unit(const StepParams& p, SharedState& sh, int u) {
   const int tid = threadIdx.x;
   const int t0 = u * p.rows_per_unit;
@@ -406,10 +432,8 @@ __device__ __forceinline__ void copy_unit(const StepParams& p, SharedState& sh, 
     sh.src[2 * tid + 1] = sh_src;
     sh.dst[2 * tid + 1] = xr + p.nvh;
   }
-  __syncthreads();
-  const int nseg = 2 * nrows;
-  constexpr int kSeg = 4;   // half rows per batch
-  constexpr int kCols = 2;  // vectors per thread per half row per batch
+  S::sync();
+  const int nseg = 2 * nrows;  // kSeg half rows x kCols vectors per thread per batch
   for (int v0 = 0; v0 < p.nvh; v0 += kCols * kThreads) {
     for (int sg = 0; sg < nseg; sg += kSeg) {
       uint4 buf[kSeg][kCols];
@@ -440,6 +464,17 @@ __device__ __forceinline__ void copy_unit(const StepParams& p, SharedState& sh, 
   }
 }
 
+// Copy tile with eight loads per thread in flight: eight half rows at a time
+// when a half row is at most one vector per thread, else four half rows of
+// two vectors.
+template <class S>
+__device__ __forceinline__ void copy_tile(const StepParams& p, SharedState& sh, int u) {
+  if (p.nvh <= kThreads)
+    copy_unit<S, 8, 1>(p, sh, u);
+  else
+    copy_unit<S, 4, 2>(p, sh, u);
+}
+
 // ------------------------------------------------------------------- kernel
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 3) step_kernel(const StepParams p) {
@@ -457,7 +492,7 @@ __global__ void __launch_bounds__(kThreads, 3) step_kernel(const StepParams p) {
     if (u < p.n_arg_units)
       argmax_unit<DT>(p, sh, u);
     else
-      copy_unit(p, sh, u - p.n_arg_units);
+      copy_tile<SyncAll>(p, sh, u - p.n_arg_units);
     __syncthreads();
     if (threadIdx.x == 0) sh.unit = (int)next;
     __syncthreads();
@@ -473,9 +508,196 @@ __global__ void __launch_bounds__(kThreads, 3) step_kernel(const StepParams p) {
   }
 }
 
+// ------------------------------------------------ pipelined (bulk-copy) kernel
+// One producer warp streams every argmax chunk into a ring of shared-memory
+// stages with cp.async.bulk (one instruction per 16 KiB, completion counted on
+// an mbarrier), running ahead across unit boundaries; eight consumer warps
+// reduce each stage from shared memory, hand it back through a second
+// mbarrier, and do the unit ends, epilogues and X tiles exactly as the
+// register-streaming kernel does.  Bytes in flight are bounded by the ring
+// (STAGES x 16 KiB per CTA), not by registers, and never stop while the
+// consumers finish a unit.
+constexpr int kTmaThreads = kThreads + 32;  // 8 consumer warps + 1 producer warp
+constexpr int kStageBytes = 16384;
+constexpr int kStageVecs = kStageBytes / 16;
+
+enum StageKind { kStageArgmax = 0, kStageCopy = 1, kStageStop = 2 };
+struct StageInfo {
+  int kind, unit, v, n, last;
+};
+
+// Producer (one thread): hand out units in order and fill the ring.
+template <int STAGES>
+__device__ __forceinline__ void produce(const StepParams& p, uint4* ring, uint64_t* full,
+                                        uint64_t* empty, StageInfo* info) {
+  const uint64_t pol = l2_evict_first_policy();
+  int stage = 0;
+  uint32_t phase = 0;
+  bool ok = true;
+  int pend[STAGES];  // parity of the last phase a copy was issued for, or -1
+#pragma unroll
+  for (int s = 0; s < STAGES; ++s) pend[s] = -1;
+  int u = blockIdx.x;
+  for (;;) {
+    const bool stop = u >= p.n_units;
+    const int next = stop ? 0 : (int)(gridDim.x + atomicAdd(p.sched, 1u));
+    if (stop || u >= p.n_arg_units) {
+      if (!(ok = mbar_wait(&empty[stage], phase ^ 1))) break;
+      info[stage] = StageInfo{stop ? kStageStop : kStageCopy, stop ? 0 : u - p.n_arg_units,
+                              0, 0, 0};
+      mbar_arrive(&full[stage]);
+      if (++stage == STAGES) {
+        stage = 0;
+        phase ^= 1;
+      }
+      if (stop) break;
+    } else {
+      const int r = u / p.C;
+      const int c = u - r * p.C;
+      const uint4* row = reinterpret_cast<const uint4*>(static_cast<const char*>(p.logits) +
+                                                        (long long)r * p.row_bytes);
+      const int v_lo = c * p.chunk_vecs;
+      const int v_hi = min(v_lo + p.chunk_vecs, p.nvec);
+      int v = v_lo;
+      do {  // a chunk with no whole vector still sends one empty piece
+        const int n = max(0, min(kStageVecs, v_hi - v));
+        if (!(ok = mbar_wait(&empty[stage], phase ^ 1))) break;
+        info[stage] = StageInfo{kStageArgmax, u, v, n, v + n >= v_hi ? 1 : 0};
+        if (n > 0) {
+          mbar_arrive_expect_tx(&full[stage], (uint32_t)n * 16u);
+          bulk_load(ring + (long long)stage * kStageVecs, row + v, (uint32_t)n * 16u,
+                    &full[stage], pol);
+          pend[stage] = (int)phase;
+        } else {
+          mbar_arrive(&full[stage]);
+        }
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+        v += kStageVecs;
+      } while (v < v_hi);
+      if (!ok) break;
+    }
+    u = next;
+  }
+  if (!ok) {
+    atomicOr(p.err, PE_ERR_TIMEOUT);
+    // let every copy already issued land before the CTA leaves (bounded)
+    for (int s = 0; s < STAGES; ++s)
+      if (pend[s] >= 0) mbar_wait(&full[s], (uint32_t)pend[s]);
+  }
+}
+
+// Consumers (eight warps): reduce stages in ring order.
+template <int DT, int STAGES>
+__device__ __forceinline__ void consume(const StepParams& p, SharedState& sh, const uint4* ring,
+                                        uint64_t* full, uint64_t* empty,
+                                        const StageInfo* info) {
+  using E = Elem<DT>;
+  const int tid = threadIdx.x;
+  const int lane = tid & 31;
+  int stage = 0;
+  uint32_t phase = 0;
+  float m = 0.f;
+  uint4 q = make_uint4(0u, 0u, 0u, 0u);
+  int qv = -1;
+  for (int iter = 0;; ++iter) {
+    // one thread waits (bounded) and tells the others, so that all consumers
+    // take the same branch and meet at the same named barriers; two slots,
+    // so thread 0 never overwrites a verdict another thread has yet to read
+    if (tid == 0) sh.verdict[iter & 1] = mbar_wait(&full[stage], phase) ? 1 : 0;
+    SyncConsumers::sync();
+    if (!sh.verdict[iter & 1]) {
+      if (tid == 0) atomicOr(p.err, PE_ERR_TIMEOUT);
+      break;
+    }
+    mbar_wait(&full[stage], phase);  // completed: returns at once, orders this thread
+    const StageInfo in = info[stage];
+    if (in.kind == kStageStop) break;
+    if (in.kind == kStageCopy) {
+      copy_unit<SyncConsumers, 8, 2>(p, sh, in.unit);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);
+    } else {
+      const uint4* buf = ring + (long long)stage * kStageVecs;
+      uint4 x[kStageVecs / kThreads];
+#pragma unroll
+      for (int k = 0; k < kStageVecs / kThreads; ++k) {
+        const int i = k * kThreads + tid;
+        x[k] = i < in.n ? buf[i] : E::neg_inf();
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[stage]);  // this warp is done with the stage
+#pragma unroll
+      for (int k = 0; k < kStageVecs / kThreads; ++k) {
+        const float vm = E::vmax(x[k]);
+        const bool valid = k * kThreads + tid < in.n;
+        if (valid && (qv < 0 || vm > m)) {  // pieces and k run in increasing column order
+          m = vm;
+          q = x[k];
+          qv = in.v + k * kThreads + tid;
+        }
+      }
+      if (in.last) {
+        const int r = in.unit / p.C;
+        const int c = in.unit - r * p.C;
+        const unsigned long long key =
+            qv >= 0 ? make_key(m, (uint32_t)(qv * E::kPerVec + E::first_equal(q, m))) : 0ull;
+        finish_argmax_unit<SyncConsumers, DT>(p, sh, r, c, key);
+        qv = -1;
+      }
+    }
+    if (++stage == STAGES) {
+      stage = 0;
+      phase ^= 1;
+    }
+  }
+}
+
+template <int DT, int STAGES, int MINB>
+__global__ void __launch_bounds__(kTmaThreads, MINB) step_kernel_tma(const StepParams p) {
+  extern __shared__ __align__(128) unsigned char ring_raw[];
+  __shared__ SharedState sh;
+  __shared__ __align__(8) uint64_t full[STAGES];
+  __shared__ __align__(8) uint64_t empty[STAGES];
+  __shared__ StageInfo info[STAGES];
+  if (p.in_offsets && !offsets_valid(p.in_offsets, p.B, p.R, p.Kp + 1)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.err, PE_ERR_OFFSETS);
+    return;
+  }
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kWarps);
+    }
+    mbar_init_fence();
+  }
+  __syncthreads();
+  if ((tid >> 5) == kWarps) {
+    if ((tid & 31) == 0)
+      produce<STAGES>(p, reinterpret_cast<uint4*>(ring_raw), full, empty, info);
+    __syncwarp();
+  } else {
+    consume<DT, STAGES>(p, sh, reinterpret_cast<const uint4*>(ring_raw), full, empty, info);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const unsigned done = atomicAdd(p.sched + 1, 1u);
+    if (done == gridDim.x - 1) {
+      atomicExch(p.sched, 0u);
+      atomicExch(p.sched + 1, 0u);
+    }
+  }
+}
+
 }  // namespace pe
 
 // ---------------------------------------------------------------- host side
+#include <atomic>
+
 namespace {
 
 using pe_host::aligned16;
@@ -507,7 +729,49 @@ void plan_argmax(pe::StepParams& p, int elt, int rows, int grid_max, int batches
   p.n_arg_units = rows * p.C;
 }
 
-int launch(const pe::StepParams& p, int dtype, int grid, cudaStream_t stream) {
+// Dynamic shared memory above 48 KiB must be opted into once per kernel and
+// device (a host-side attribute; no synchronisation).
+template <class K>
+bool allow_smem(K kernel, int bytes, std::atomic<unsigned long long>& done_mask) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  const unsigned long long bit = 1ull << dev;
+  if (done_mask.load(std::memory_order_relaxed) & bit) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+      cudaSuccess)
+    return false;
+  done_mask.fetch_or(bit);
+  return true;
+}
+
+template <int DT, int STAGES, int MINB>
+int launch_tma(const pe::StepParams& p, int grid, cudaStream_t stream) {
+  static std::atomic<unsigned long long> attr_done{0};
+  const int smem = STAGES * pe::kStageBytes;
+  if (!allow_smem(pe::step_kernel_tma<DT, STAGES, MINB>, smem, attr_done)) return PE_ECUDA;
+  pe::step_kernel_tma<DT, STAGES, MINB><<<grid, pe::kTmaThreads, smem, stream>>>(p);
+  return pe_host::launch_status();
+}
+
+// Grid of the chosen kernel variant: register streaming (ctas_per_sm CTAs
+// of 256 threads per SM) or the bulk-copy pipeline (1 CTA with a 12-stage
+// ring, or 2 CTAs with 6 stages each, per SM).
+int grid_max_for(const pe_host::Tuning& tn, const pe_host::DeviceInfo& dev) {
+  if (tn.variant == 2) return dev.sm_count * (tn.ctas_per_sm >= 2 ? 2 : 1);
+  return dev.sm_count * tn.ctas_per_sm;
+}
+
+
+int launch(const pe::StepParams& p, int dtype, int grid, const pe_host::Tuning& tn,
+           cudaStream_t stream) {
+  if (tn.variant == 2) {
+    const bool two = tn.ctas_per_sm >= 2;
+    if (dtype == PE_BF16)
+      return two ? launch_tma<PE_BF16, 6, 2>(p, grid, stream)
+                 : launch_tma<PE_BF16, 12, 1>(p, grid, stream);
+    return two ? launch_tma<PE_F32, 6, 2>(p, grid, stream)
+               : launch_tma<PE_F32, 12, 1>(p, grid, stream);
+  }
   if (dtype == PE_BF16)
     pe::step_kernel<PE_BF16><<<grid, pe::kThreads, 0, stream>>>(p);
   else
@@ -559,12 +823,12 @@ int pe_verify_greedy(const void* logits, int dtype, int64_t row_stride, int32_t 
   p.target_argmax = target_argmax;
   p.err = err;
   const int rows = B * (Kp + 1);
-  const int grid_max = dev.sm_count * tn.ctas_per_sm;
+  const int grid_max = grid_max_for(tn, dev);
   plan_argmax(p, elt, rows, grid_max, tn.chunk_batches);
   p.n_units = p.n_arg_units;
   bind_workspace(p, workspace, rows, B);
   const int grid = p.n_units < grid_max ? p.n_units : grid_max;
-  return launch(p, dtype, grid, static_cast<cudaStream_t>(stream));
+  return launch(p, dtype, grid, tn, static_cast<cudaStream_t>(stream));
 }
 
 int pe_step(const pe_step_args* a, void* stream) {
@@ -641,14 +905,14 @@ int pe_step(const pe_step_args* a, void* stream) {
   p.X = static_cast<uint4*>(a->X);
   p.err = a->err;
   const int rows = B * (Kp + 1);
-  const int grid_max = dev.sm_count * tn.ctas_per_sm;
+  const int grid_max = grid_max_for(tn, dev);
   plan_argmax(p, elt, rows, grid_max, tn.chunk_batches);
   p.rows_per_unit = tn.rows_per_unit;
   p.n_copy_units = (p.T + p.rows_per_unit - 1) / p.rows_per_unit;
   p.n_units = p.n_arg_units + p.n_copy_units;
   bind_workspace(p, a->workspace, rows, B);
   const int grid = p.n_units < grid_max ? p.n_units : grid_max;
-  return launch(p, a->logits_dtype, grid, static_cast<cudaStream_t>(stream));
+  return launch(p, a->logits_dtype, grid, tn, static_cast<cudaStream_t>(stream));
 }
 
 }  // extern "C"

@@ -32,6 +32,23 @@ def _gen(spec, seed):
     return wl.make_workload(spec, seed, device="cuda")
 
 
+class tuned:
+    """Run a block under other launch-shape knobs, then restore them."""
+    def __init__(self, **kw):
+        self.kw = kw
+
+    def __enter__(self):
+        self.before = _native.get_tuning()
+        _native.set_tuning(**self.kw)
+
+    def __exit__(self, *exc):
+        _native.set_tuning(**self.before)
+
+
+VARIANTS = [dict(variant=1), dict(variant=2)]
+VARIANT_IDS = ["regs", "pipeline"]
+
+
 # ------------------------------------------------------------ full sizes
 
 FULL = [("tiny", s) for s in range(4)] + [("decode_b1", 0), ("decode_b1", 1),
@@ -39,11 +56,13 @@ FULL = [("tiny", s) for s in range(4)] + [("decode_b1", 0), ("decode_b1", 1),
                                           ("decode_b256", 0)]
 
 
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
 @pytest.mark.parametrize("name,trial", FULL, ids=lambda v: str(v))
-def test_fused_step_full_size(name, trial):
+def test_fused_step_full_size(name, trial, variant):
     cfg = list(wl.SPECS).index(name) + 1
     w = _gen(name, 1000 * cfg + trial)
-    got = run_fused(w)
+    with tuned(**variant):
+        got = run_fused(w)
     ref = oracle_of(w)
     assert_same(got, ref, what=name)
     if not w.spec.prefill:  # the planted lengths are what any verifier must find
@@ -75,16 +94,26 @@ def _variants():
     return out
 
 
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
 @pytest.mark.parametrize("spec", _variants(), ids=lambda s: s.name)
-def test_fused_step_variants(spec):
+def test_fused_step_variants(spec, variant):
     for seed in (0, 1):
         w = _gen(spec, seed)
-        assert_same(run_fused(w), oracle_of(w), what=spec.name)
+        with tuned(**variant):
+            got = run_fused(w)
+        assert_same(got, oracle_of(w), what=spec.name)
 
 
 @pytest.mark.parametrize("tuning", [dict(), dict(ctas_per_sm=1), dict(chunk_batches=1),
                                     dict(ctas_per_sm=2, chunk_batches=2, rows_per_unit=16),
-                                    dict(rows_per_unit=1)],
+                                    dict(rows_per_unit=1),
+                                    dict(variant=2, ctas_per_sm=1),
+                                    dict(variant=2, ctas_per_sm=2),
+                                    dict(variant=2, ctas_per_sm=1, chunk_batches=1,
+                                         rows_per_unit=16),
+                                    dict(variant=2, ctas_per_sm=2, chunk_batches=16,
+                                         rows_per_unit=1),
+                                    ],
                          ids=lambda d: ",".join("%s=%d" % kv for kv in d.items()) or "default")
 def test_launch_shapes_do_not_change_results(tuning):
     before = _native.get_tuning()
@@ -136,8 +165,10 @@ def _tie_rows(V, dtype):
                                          (65537, torch.float32, 3),
                                          (1000, torch.float32, 0),
                                          (9, torch.bfloat16, 7)])
-@pytest.mark.parametrize("tuning", [dict(), dict(ctas_per_sm=1, chunk_batches=1)],
-                         ids=["default", "coarse"])
+@pytest.mark.parametrize("tuning", [dict(), dict(ctas_per_sm=1, chunk_batches=1),
+                                    dict(variant=2, ctas_per_sm=1),
+                                    dict(variant=2, ctas_per_sm=2, chunk_batches=1)],
+                         ids=["default", "coarse", "pipeline", "pipeline_fine"])
 def test_verify_argmax_ties(V, dtype, pad, tuning):
     rows = _tie_rows(V, dtype)
     ref = oracle.argmax_rows(rows)
