@@ -66,6 +66,7 @@ typedef enum pe_dtype { PE_F32 = 0, PE_BF16 = 1 } pe_dtype;
 #define PE_ERR_SLOT_RANGE 4u  /* accepted_len outside [0,Kp]: taken as 0    */
 #define PE_ERR_OFFSETS 8u     /* in_offsets invalid: nothing is written     */
 #define PE_ERR_MAP_RANGE 16u  /* hidden_map entry outside [0,T): skipped    */
+#define PE_ERR_ROW_RANGE 64u  /* readout row index outside [0,rows): -1     */
 #define PE_ERR_TIMEOUT 32u    /* a bounded pipeline wait gave up (outputs
                                  incomplete; never expected)               */
 
@@ -73,7 +74,8 @@ typedef enum pe_dtype { PE_F32 = 0, PE_BF16 = 1 } pe_dtype;
 #define PE_MAX_KP 255 /* previous draft depth K'  */
 #define PE_MAX_K 256  /* new draft depth K        */
 
-/* Bytes of scratch that pe_verify_greedy / pe_step need for a batch with
+/* Bytes of scratch that pe_verify_greedy, pe_draft_readout (with
+ * logits_rows = B = n), pe_step and pe_step_early_exit need for a batch with
  * `logits_rows` = B*(Kp+1) logits rows and B requests.  The caller
  * allocates it once, zero-filled, and may reuse it for every later call of
  * any size up to those; each call leaves it zeroed again on completion.
@@ -97,6 +99,24 @@ int pe_verify_greedy(const void* logits, int dtype, int64_t row_stride,
                      int32_t* accepted_len, int32_t* bonus_token,
                      int32_t* target_argmax, void* workspace, uint32_t* err,
                      void* stream);
+
+/* Drafter readout [P2 Step 2: all positions pass through the drafter's N
+ * layers and LM head, which predicts t_1..t_K]: greedy draft tokens.
+ *   out_tokens[i] = argmax over the first V columns of logits row
+ *                   sample_idx[i] (row i when sample_idx is NULL), lowest
+ *                   column on ties
+ *  logits      [rows, V'] of `dtype`, row stride `row_stride` elements:
+ *              either the drafter's logits for every output slot ([T, V],
+ *              read through sample_idx from pe_build_draft_batch) or only for
+ *              the sampled rows ([B*K, V], sample_idx NULL).
+ *  sample_idx  [n] int32 or NULL (then n <= rows).  An index outside
+ *              [0, rows) gives out_tokens[i] = -1 and PE_ERR_ROW_RANGE.
+ *  workspace   pe_workspace_bytes(n, n) bytes, zeroed (as for pe_step).
+ * n == 0 enqueues nothing. */
+int pe_draft_readout(const void* logits, int dtype, int64_t row_stride,
+                     int32_t rows, int32_t V, const int32_t* sample_idx,
+                     int32_t n, int32_t* out_tokens, void* workspace,
+                     uint32_t* err, void* stream);
 
 /* Draft-batch rebuild [P2 Fused Triton Kernel; KV Cache and CUDA Graphs].
  * For request b with bonus slot s_b = n_b-1-Kp+a_b and slot k of its output
@@ -196,6 +216,17 @@ typedef struct pe_step_args {
 } pe_step_args;
 
 int pe_step(const pe_step_args* args /* host */, void* stream);
+
+/* The whole step with early exit [P1 quick-read: acceptance length]: the
+ * verified rows of a request are read in order and the rows after its
+ * first mismatch are not read at all (rows of every request are streamed
+ * row 0 first, then row 1, ...; a chunk whose request already has a known
+ * earlier mismatch is skipped).  Every output equals pe_step's, except
+ * target_argmax, which holds each request's rows 0..a_b and -1 for the rows
+ * after a_b.  Same arguments and workspace as pe_step; Kp <= 31 (one bit per
+ * verified row), else PE_EINVAL.  Always runs the register-streaming kernel
+ * (pe_tuning.variant does not apply). */
+int pe_step_early_exit(const pe_step_args* args /* host */, void* stream);
 
 /* pe_step for callers that cannot allocate device memory at all, not even
  * the small scratch above: code running under a memory manager that owns

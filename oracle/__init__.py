@@ -29,6 +29,7 @@ ERR_BLOCK_RANGE = 2
 ERR_SLOT_RANGE = 4
 ERR_OFFSETS = 8
 ERR_MAP_RANGE = 16
+ERR_ROW_RANGE = 64
 
 _lock = threading.Lock()
 _libs: dict = {}
@@ -81,6 +82,7 @@ def _load():
             lib.oracle_argmax_rows.argtypes = [P, c_int, i64, i32, i32, P]
             lib.oracle_verify_greedy.argtypes = [P, c_int, i64, i32, i32, i32,
                                                  P, P, P, P]
+            lib.oracle_draft_readout.argtypes = [P, c_int, i64, i32, i32, P, i32, P, P]
             lib.oracle_build_draft_batch.argtypes = (
                 [i32, i32, i32, i32, P, P, P, P, P, P, i32, i32] + [P] * 9)
             lib.oracle_assemble_draft_inputs.argtypes = (
@@ -89,6 +91,7 @@ def _load():
                 [c_int, c_int, i32, i32, i32, i32, i32, i32, P, i64, P, P, P, P,
                  i32, i32, P, P, P] + [P] * 13)
             for fn in (lib.oracle_argmax_rows, lib.oracle_verify_greedy,
+                       lib.oracle_draft_readout,
                        lib.oracle_build_draft_batch,
                        lib.oracle_assemble_draft_inputs, lib.oracle_step):
                 fn.restype = ctypes.c_int
@@ -132,6 +135,23 @@ def argmax_rows(logits: torch.Tensor, V: int | None = None) -> torch.Tensor:
     _check(lib.oracle_argmax_rows(_ptr(logits), _dt(logits), logits.stride(0),
                                   logits.shape[0], V, _ptr(out)), "argmax_rows")
     return out
+
+
+def draft_readout(logits, sample_idx=None, n=None):
+    """Greedy draft tokens: argmax of logits row sample_idx[i] (row i when
+    sample_idx is None).  Returns (tokens[n], error word)."""
+    lib = _load()
+    logits = logits.detach().cpu()
+    assert logits.dim() == 2 and logits.stride(1) == 1
+    idx = _i32(sample_idx)
+    if n is None:
+        n = idx.numel() if idx is not None else logits.shape[0]
+    out = torch.empty(n, dtype=torch.int32)
+    err = ctypes.c_uint32(0)
+    _check(lib.oracle_draft_readout(_ptr(logits), _dt(logits), logits.stride(0),
+                                    logits.shape[0], logits.shape[1], _ptr(idx), n,
+                                    _ptr(out), ctypes.byref(err)), "draft_readout")
+    return out, err.value
 
 
 def verify_greedy(logits, B, Kp, V, tokens):

@@ -77,6 +77,30 @@ int oracle_argmax_rows(const void* logits, int dtype, int64_t row_stride,
   return 0;
 }
 
+/* ---- drafter readout: greedy t_1..t_K from the drafter's logits -------- */
+/* "P-EAGLE: Parallel Speculative Decoding in vLLM" -- Step 2: the LM head
+   predicts draft tokens t_1..t_K; greedy drafting takes each row's argmax. */
+
+int oracle_draft_readout(const void* logits, int dtype, int64_t row_stride,
+                         int32_t rows, int32_t V, const int32_t* sample_idx,
+                         int32_t n, int32_t* out, uint32_t* err) {
+  int32_t i;
+  if (rows < 0 || V < 1 || n < 0 || !err) return -1;
+  if (n > 0 && (!logits || !out)) return -1;
+  for (i = 0; i < n; ++i) {
+    int32_t r = sample_idx ? sample_idx[i] : i;
+    if (r < 0 || r >= rows) {
+      *err |= ORC_ERR_ROW_RANGE;
+      out[i] = -1;
+      continue;
+    }
+    oracle_argmax_rows((const char*)logits +
+                           (int64_t)r * row_stride * elt_of(dtype),
+                       dtype, row_stride, 1, V, &out[i]);
+  }
+  return 0;
+}
+
 /* ---- a2: greedy acceptance and bonus token ---------------------------- */
 
 int oracle_verify_greedy(const void* logits, int dtype, int64_t row_stride,

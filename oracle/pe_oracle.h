@@ -27,10 +27,18 @@ extern "C" {
 #define ORC_ERR_SLOT_RANGE 4u  /* accepted length outside [0, K']            */
 #define ORC_ERR_OFFSETS 8u     /* segment offsets are not a valid partition  */
 #define ORC_ERR_MAP_RANGE 16u  /* hidden-state mapping outside [0, T)        */
+#define ORC_ERR_ROW_RANGE 64u  /* readout row index outside [0, rows)        */
 
 /* Row argmax, lowest index on ties, -0.0 == +0.0.  out[rows]. */
 int oracle_argmax_rows(const void* logits, int dtype, int64_t row_stride,
                        int32_t rows, int32_t V, int32_t* out);
+
+/* Greedy drafter readout: out[i] = argmax of logits row sample_idx[i]
+ * (row i when sample_idx is NULL), lowest index on ties; an index outside
+ * [0, rows) gives -1 and raises ORC_ERR_ROW_RANGE. */
+int oracle_draft_readout(const void* logits, int dtype, int64_t row_stride,
+                         int32_t rows, int32_t V, const int32_t* sample_idx,
+                         int32_t n, int32_t* out, uint32_t* err);
 
 /* Greedy verification over logits[B*(Kp+1), V] (row r of request b is
  * b*(Kp+1)+j).  tokens[B*(Kp+1)]: row j+1 of request b holds draft d_{j+1}.

@@ -25,11 +25,14 @@ ERR_SLOT_RANGE = 4
 ERR_OFFSETS = 8
 ERR_MAP_RANGE = 16
 ERR_TIMEOUT = 32
+ERR_ROW_RANGE = 64
 MAX_KP, MAX_K = 255, 256
 
 # every function the C header declares
-EXPORTS = ("pe_workspace_bytes", "pe_verify_greedy", "pe_build_draft_batch",
-           "pe_assemble_draft_inputs", "pe_step", "pe_step_noalloc", "pe_get_tuning",
+EXPORTS = ("pe_workspace_bytes", "pe_verify_greedy", "pe_draft_readout",
+           "pe_build_draft_batch",
+           "pe_assemble_draft_inputs", "pe_step", "pe_step_early_exit", "pe_step_noalloc",
+           "pe_get_tuning",
            "pe_set_tuning", "pe_status_str")
 
 
@@ -88,10 +91,14 @@ def load():
         lib.pe_workspace_bytes.restype = ctypes.c_size_t
         lib.pe_verify_greedy.argtypes = [P, ctypes.c_int, i64, i32, i32, i32, P, P, P,
                                          P, P, P, P]
+        lib.pe_draft_readout.argtypes = [P, ctypes.c_int, i64, i32, i32, P, i32, P, P, P, P]
+        lib.pe_draft_readout.restype = ctypes.c_int
         lib.pe_build_draft_batch.argtypes = ([i32, i32, i32, i32, i32, P, P, P, P, P, P,
                                               i32, i32] + [P] * 10)
         lib.pe_assemble_draft_inputs.argtypes = [ctypes.c_int, i32, i32, i32, i32] + [P] * 9
         lib.pe_step.argtypes = [ctypes.POINTER(StepArgs), P]
+        lib.pe_step_early_exit.argtypes = [ctypes.POINTER(StepArgs), P]
+        lib.pe_step_early_exit.restype = ctypes.c_int
         lib.pe_step_noalloc.argtypes = [ctypes.POINTER(StepArgs), P]
         lib.pe_step_noalloc.restype = ctypes.c_int
         lib.pe_get_tuning.argtypes = [ctypes.POINTER(Tuning)]
@@ -178,6 +185,21 @@ def verify_greedy(logits, Kp, in_tokens, accepted_len, bonus_token, workspace, e
         _dev(workspace, "workspace", torch.uint8, workspace_bytes(rows, B)),
         _dev(err, "err", torch.int32, 1), _stream(stream))
     _check(lib, rc, "pe_verify_greedy")
+
+
+def draft_readout(logits, out_tokens, workspace, err, sample_idx=None, stream=None):
+    """Greedy draft tokens: argmax of logits row sample_idx[i] (row i when
+    sample_idx is None) into out_tokens[i]."""
+    lib = load()
+    lp, dt, stride = _logits(logits)
+    rows, V = logits.shape
+    n = sample_idx.numel() if sample_idx is not None else out_tokens.numel()
+    rc = lib.pe_draft_readout(
+        lp, dt, stride, rows, V, _dev(sample_idx, "sample_idx", torch.int32, n), n,
+        _dev(out_tokens, "out_tokens", torch.int32, n),
+        _dev(workspace, "workspace", torch.uint8, workspace_bytes(n, n)),
+        _dev(err, "err", torch.int32, 1), _stream(stream))
+    _check(lib, rc, "pe_draft_readout")
 
 
 @dataclass
@@ -312,6 +334,14 @@ def step_packed(args: StepArgs, stream=None):
     """Launch the fused step from a packed argument block."""
     lib = load()
     _check(lib, lib.pe_step(ctypes.byref(args), _stream(stream)), "pe_step")
+
+
+def step_early_exit_packed(args: StepArgs, stream=None):
+    """The fused step with early exit (rows after each request's first
+    mismatch are not read; target_argmax holds -1 for them)."""
+    lib = load()
+    _check(lib, lib.pe_step_early_exit(ctypes.byref(args), _stream(stream)),
+           "pe_step_early_exit")
 
 
 def step(**kw):

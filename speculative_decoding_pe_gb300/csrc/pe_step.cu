@@ -53,6 +53,8 @@ struct StepParams {
   int chunk_vecs, C, Rl;  // argmax chunking: vectors per chunk, chunks per row, rows
   int n_arg_units, rows_per_unit, n_copy_units, n_units;
   const void* logits;
+  const int32_t* row_index;  // logits row of argmax row r (NULL: r itself)
+  int rows_total;            // logits rows addressable through row_index
   const int32_t* in_offsets;
   const int32_t* in_tokens;
   const int32_t* in_positions;
@@ -75,6 +77,9 @@ struct StepParams {
   uint32_t* sched;
   uint32_t* count;
   unsigned long long* keys;
+  unsigned long long* state;  // early exit: per-request done / match bits
+  uint32_t* rcount;           // early exit: finished chunks per row
+  int32_t* amax_ws;           // early exit: argmax of each completed row
   uint32_t* err;
 };
 
@@ -85,6 +90,7 @@ struct SharedState {
   int unit;
   int last;
   int first;
+  int skip;
   int verdict[2];
   int amax[PE_MAX_KP + 1];
   int tok[PE_MAX_KP + 1];
@@ -93,6 +99,14 @@ struct SharedState {
   uint4* dst[2 * kMaxRowsPerUnit];
   int mode[2 * kMaxRowsPerUnit];
 };
+
+// Logits row read for argmax row r, or nullptr when an index given through
+// row_index is outside [0, rows_total).
+__device__ __forceinline__ const char* logits_row(const StepParams& p, int r) {
+  const int pr = p.row_index ? __ldg(p.row_index + r) : r;
+  if (pr < 0 || pr >= p.rows_total) return nullptr;
+  return static_cast<const char*>(p.logits) + (long long)pr * p.row_bytes;
+}
 
 __device__ __forceinline__ int seg_begin(const StepParams& p, int b) {
   return p.in_offsets ? __ldg(p.in_offsets + b) : b * (p.Kp + 1);
@@ -181,9 +195,12 @@ struct Elem<PE_F32> {
 // verified rows, all at once; (2) after the verdict, the embedding rows of
 // the verified slots with their final tokens and the block-table entries of
 // the kept slots.
-template <class S>
+// EARLY: the accepted length `a_known` is already settled (early-exit step);
+// rows 0..a_known are read from the completed-row results and later rows,
+// which may never have been read, report -1.
+template <class S, bool EARLY = false>
 __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedState& sh,
-                                                 int b) {
+                                                 int b, int a_known = -1) {
   const int tid = threadIdx.x;
   const int Kp = p.Kp;
   const int nr = Kp + 1;  // verified rows (<= 256 = threads)
@@ -191,25 +208,29 @@ __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedStat
   const int n = seg_begin(p, b + 1) - io;
   const int vb = n - 1 - Kp;  // segment row of the first verified row
   if (tid < nr) {
-    const unsigned long long k = atomicExch(p.keys + (long long)b * nr + tid, 0ull);
-    sh.amax[tid] = (int)key_col(k);
+    if (EARLY) {
+      sh.amax[tid] = tid <= a_known ? __ldcg(p.amax_ws + (long long)b * nr + tid) : -1;
+    } else {
+      const unsigned long long k = atomicExch(p.keys + (long long)b * nr + tid, 0ull);
+      sh.amax[tid] = (int)key_col(k);
+    }
     if (tid < Kp) sh.tok[tid] = __ldg(p.in_tokens + io + vb + tid + 1);  // draft d_{tid+1}
     if (p.full) sh.pos[tid] = __ldg(p.in_positions + io + vb + tid);
   }
   if (tid == 0) {
-    sh.first = Kp;
-    atomicExch(p.count + b, 0u);
+    sh.first = EARLY ? a_known : Kp;
+    if (!EARLY) atomicExch(p.count + b, 0u);
   }
   S::sync();
   // accepted length: first draft that differs from the target's choice
-  if (tid < Kp && sh.amax[tid] != sh.tok[tid]) atomicMin(&sh.first, tid);
+  if (!EARLY && tid < Kp && sh.amax[tid] != sh.tok[tid]) atomicMin(&sh.first, tid);
   if (p.target_argmax && tid < nr) p.target_argmax[(long long)b * nr + tid] = sh.amax[tid];
   S::sync();
   const int a = sh.first;
   const int bonus = sh.amax[a];
   if (!p.full) {
     if (tid == 0) {
-      p.accepted_len[b] = a;
+      if (p.accepted_len) p.accepted_len[b] = a;
       p.bonus_token[b] = bonus;
     }
     return;
@@ -284,22 +305,17 @@ __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedStat
 // ------------------------------------------------------------- argmax chunk
 template <class S, int DT>
 __device__ __forceinline__ void finish_argmax_unit(const StepParams& p, SharedState& sh, int r,
-                                                   int c, unsigned long long key);
+                                                   int c, const char* rowp,
+                                                   unsigned long long key);
 
+// Key (value, first column) of this thread's elements of vectors
+// [v_lo, v_hi) of one logits row.  Elements are visited in increasing column
+// order (batch, then vector i, then element), so a strict '>' keeps the
+// first occurrence.
 template <int DT>
-__device__ __forceinline__ void argmax_unit(const StepParams& p, SharedState& sh, int u) {
+__device__ __forceinline__ unsigned long long thread_key(const uint4* row, int v_lo, int v_hi) {
   using E = Elem<DT>;
   const int tid = threadIdx.x;
-  const int r = u / p.C;
-  const int c = u - r * p.C;
-  const char* rowp = static_cast<const char*>(p.logits) + (long long)r * p.row_bytes;
-  const uint4* row = reinterpret_cast<const uint4*>(rowp);
-  const int v_lo = c * p.chunk_vecs;
-  const int v_hi = min(v_lo + p.chunk_vecs, p.nvec);
-
-  // Running maximum of this thread's elements and the column of its first
-  // occurrence.  Elements are visited in increasing column order (batch,
-  // then vector i, then element), so a strict '>' keeps the first one.
   float m = 0.f;
   int col = -1;
   for (int base = v_lo; base < v_hi; base += kBatchVecs) {
@@ -330,8 +346,21 @@ __device__ __forceinline__ void argmax_unit(const StepParams& p, SharedState& sh
       col = (base + vi * kThreads + tid) * E::kPerVec + E::first_equal(q, gm);
     }
   }
-  const unsigned long long key = col >= 0 ? make_key(m, (uint32_t)col) : 0ull;
-  finish_argmax_unit<SyncAll, DT>(p, sh, r, c, key);
+  return col >= 0 ? make_key(m, (uint32_t)col) : 0ull;
+}
+
+template <int DT>
+__device__ __forceinline__ void argmax_unit(const StepParams& p, SharedState& sh, int u) {
+  const int tid = threadIdx.x;
+  const int r = u / p.C;
+  const int c = u - r * p.C;
+  const char* rowp = logits_row(p, r);
+  const int v_lo = c * p.chunk_vecs;
+  const int v_hi = rowp ? min(v_lo + p.chunk_vecs, p.nvec) : v_lo;  // bad index: nothing
+  if (!rowp && c == 0 && tid == 0) atomicOr(p.err, PE_ERR_ROW_RANGE);
+  const unsigned long long key =
+      thread_key<DT>(reinterpret_cast<const uint4*>(rowp), v_lo, v_hi);
+  finish_argmax_unit<SyncAll, DT>(p, sh, r, c, rowp, key);
 }
 
 // End of an argmax unit: fold in the leftover elements, reduce the threads'
@@ -339,12 +368,12 @@ __device__ __forceinline__ void argmax_unit(const StepParams& p, SharedState& sh
 // whose unit completes the request.
 template <class S, int DT>
 __device__ __forceinline__ void finish_argmax_unit(const StepParams& p, SharedState& sh, int r,
-                                                   int c, unsigned long long key) {
+                                                   int c, const char* rowp,
+                                                   unsigned long long key) {
   using E = Elem<DT>;
   const int tid = threadIdx.x;
-  const char* rowp = static_cast<const char*>(p.logits) + (long long)r * p.row_bytes;
   // leftover elements past the last whole vector (last chunk, one thread)
-  if (p.tail && c == p.C - 1 && tid == 0) {
+  if (p.tail && rowp && c == p.C - 1 && tid == 0) {
     const int c0 = p.nvec * E::kPerVec;
     float tm = E::scalar(rowp, c0);
     int tc = c0;
@@ -378,6 +407,102 @@ __device__ __forceinline__ void finish_argmax_unit(const StepParams& p, SharedSt
   if (last >= 0) {
     __threadfence();
     request_epilogue<S>(p, sh, last);
+  }
+}
+
+// ------------------------------------------------------- early-exit units
+// Early exit reads a request's rows in order and stops after the first
+// mismatch.  Units run row-major over (row j, request b, chunk c), so every
+// request's row 0 streams first, then row 1, ...; a unit whose request is
+// already known to mismatch at an earlier row reads nothing.  The CTA that
+// completes a row records its argmax and ORs two bits into the request's
+// state word (row done; row's argmax equals the draft).  The OR after which
+// the rows 0..a are all done, 0..a-1 all match and a mismatches (or a = K')
+// settles the request: exactly one CTA sees that change, and it runs the
+// epilogue.  Nothing ever waits for another CTA.
+
+// Accepted length settled by a state word, or -1 while it is still open.
+__device__ __forceinline__ int settled(unsigned long long st, int Kp) {
+  for (int j = 0; j <= Kp; ++j) {
+    if (!((st >> j) & 1ull)) return -1;               // row j not done yet
+    if (j == Kp || !((st >> (32 + j)) & 1ull)) return j;  // bonus row / mismatch
+  }
+  return -1;
+}
+
+template <int DT>
+__device__ __forceinline__ void argmax_unit_early(const StepParams& p, SharedState& sh, int u) {
+  using E = Elem<DT>;
+  const int tid = threadIdx.x;
+  const int per_row = p.B * p.C;
+  const int j = u / per_row;
+  const int rem = u - j * per_row;
+  const int b = rem / p.C;
+  const int c = rem - b * p.C;
+  const int r = b * (p.Kp + 1) + j;
+  if (tid == 0) {  // a mismatch already known at an earlier row makes this row moot
+    const unsigned long long st = __ldcg(p.state + b);
+    const unsigned done = (unsigned)st;
+    const unsigned match = (unsigned)(st >> 32);
+    sh.skip = (done & ~match & ((1u << j) - 1u)) != 0u;
+  }
+  __syncthreads();
+  if (sh.skip) return;
+  const char* rowp = logits_row(p, r);
+  const int v_lo = c * p.chunk_vecs;
+  const int v_hi = min(v_lo + p.chunk_vecs, p.nvec);
+  unsigned long long key = thread_key<DT>(reinterpret_cast<const uint4*>(rowp), v_lo, v_hi);
+  if (p.tail && c == p.C - 1 && tid == 0) {  // leftover elements past the last vector
+    const int c0 = p.nvec * E::kPerVec;
+    float tm = E::scalar(rowp, c0);
+    int tc = c0;
+    for (int e = 1; e < p.tail; ++e) {
+      const float x = E::scalar(rowp, c0 + e);
+      if (x > tm) {
+        tm = x;
+        tc = c0 + e;
+      }
+    }
+    const unsigned long long tk = make_key(tm, (uint32_t)tc);
+    key = tk > key ? tk : key;
+  }
+  key = warp_max_key(key);
+  if ((tid & 31) == 0) sh.red[tid >> 5] = key;
+  __syncthreads();
+  if (tid < 32) {
+    unsigned long long k = tid < kWarps ? sh.red[tid] : 0ull;
+    k = warp_max_key(k);
+    if (tid == 0) {
+      int due = -1, a = -1;
+      atomicMax(p.keys + r, k);
+      __threadfence();
+      if (atomicAdd(p.rcount + r, 1u) == (unsigned)(p.C - 1)) {  // row r complete
+        const unsigned long long kk = atomicExch(p.keys + r, 0ull);
+        atomicExch(p.rcount + r, 0u);
+        const int am = (int)key_col(kk);
+        p.amax_ws[r] = am;
+        const int io = seg_begin(p, b);
+        const int vb = seg_begin(p, b + 1) - io - 1 - p.Kp;
+        const bool match = j < p.Kp && am == __ldg(p.in_tokens + io + vb + j + 1);
+        const unsigned long long bits = (1ull << j) | (match ? (1ull << (32 + j)) : 0ull);
+        __threadfence();  // the row's argmax is visible before its done bit
+        const unsigned long long old = atomicOr(p.state + b, bits);
+        const int a_new = settled(old | bits, p.Kp);
+        if (settled(old, p.Kp) < 0 && a_new >= 0) {
+          due = b;
+          a = a_new;
+        }
+      }
+      sh.last = due;
+      sh.first = a;
+    }
+  }
+  __syncthreads();
+  const int due = sh.last;
+  const int a = sh.first;
+  if (due >= 0) {
+    __threadfence();
+    request_epilogue<SyncAll, true>(p, sh, due, a);
   }
 }
 
@@ -476,7 +601,7 @@ __device__ __forceinline__ void copy_tile(const StepParams& p, SharedState& sh, 
 }
 
 // ------------------------------------------------------------------- kernel
-template <int DT>
+template <int DT, bool EARLY>
 __global__ void __launch_bounds__(kThreads, 3) step_kernel(const StepParams p) {
   __shared__ SharedState sh;
   if (p.in_offsets && !offsets_valid(p.in_offsets, p.B, p.R, p.Kp + 1)) {
@@ -489,9 +614,12 @@ __global__ void __launch_bounds__(kThreads, 3) step_kernel(const StepParams p) {
   while (u < p.n_units) {
     unsigned next = 0;
     if (threadIdx.x == 0) next = gridDim.x + atomicAdd(p.sched, 1u);  // prefetch
-    if (u < p.n_arg_units)
-      argmax_unit<DT>(p, sh, u);
-    else
+    if (u < p.n_arg_units) {
+      if (EARLY)
+        argmax_unit_early<DT>(p, sh, u);
+      else
+        argmax_unit<DT>(p, sh, u);
+    } else
       copy_tile<SyncAll>(p, sh, u - p.n_arg_units);
     __syncthreads();
     if (threadIdx.x == 0) sh.unit = (int)next;
@@ -501,9 +629,21 @@ __global__ void __launch_bounds__(kThreads, 3) step_kernel(const StepParams p) {
   if (threadIdx.x == 0) {
     __threadfence();
     const unsigned done = atomicAdd(p.sched + 1, 1u);
-    if (done == gridDim.x - 1) {  // every CTA has taken its last unit
+    sh.last = done == gridDim.x - 1;  // every other CTA has left
+    if (sh.last) {
       atomicExch(p.sched, 0u);
       atomicExch(p.sched + 1, 0u);
+    }
+  }
+  if (EARLY) {  // the last CTA clears partly read rows and the row results
+    __syncthreads();
+    if (sh.last) {
+      for (int i = threadIdx.x; i < p.Rl; i += kThreads) {
+        p.keys[i] = 0ull;
+        p.rcount[i] = 0u;
+        p.amax_ws[i] = 0;
+      }
+      for (int i = threadIdx.x; i < p.B; i += kThreads) p.state[i] = 0ull;
     }
   }
 }
@@ -554,10 +694,11 @@ __device__ __forceinline__ void produce(const StepParams& p, uint4* ring, uint64
     } else {
       const int r = u / p.C;
       const int c = u - r * p.C;
-      const uint4* row = reinterpret_cast<const uint4*>(static_cast<const char*>(p.logits) +
-                                                        (long long)r * p.row_bytes);
+      const char* rowp = logits_row(p, r);
+      const uint4* row = reinterpret_cast<const uint4*>(rowp);
       const int v_lo = c * p.chunk_vecs;
-      const int v_hi = min(v_lo + p.chunk_vecs, p.nvec);
+      const int v_hi = rowp ? min(v_lo + p.chunk_vecs, p.nvec) : v_lo;  // bad index: nothing
+      if (!rowp && c == 0) atomicOr(p.err, PE_ERR_ROW_RANGE);
       int v = v_lo;
       do {  // a chunk with no whole vector still sends one empty piece
         const int n = max(0, min(kStageVecs, v_hi - v));
@@ -644,7 +785,7 @@ __device__ __forceinline__ void consume(const StepParams& p, SharedState& sh, co
         const int c = in.unit - r * p.C;
         const unsigned long long key =
             qv >= 0 ? make_key(m, (uint32_t)(qv * E::kPerVec + E::first_equal(q, m))) : 0ull;
-        finish_argmax_unit<SyncConsumers, DT>(p, sh, r, c, key);
+        finish_argmax_unit<SyncConsumers, DT>(p, sh, r, c, logits_row(p, r), key);
         qv = -1;
       }
     }
@@ -773,9 +914,17 @@ int launch(const pe::StepParams& p, int dtype, int grid, const pe_host::Tuning& 
                : launch_tma<PE_F32, 12, 1>(p, grid, stream);
   }
   if (dtype == PE_BF16)
-    pe::step_kernel<PE_BF16><<<grid, pe::kThreads, 0, stream>>>(p);
+    pe::step_kernel<PE_BF16, false><<<grid, pe::kThreads, 0, stream>>>(p);
   else
-    pe::step_kernel<PE_F32><<<grid, pe::kThreads, 0, stream>>>(p);
+    pe::step_kernel<PE_F32, false><<<grid, pe::kThreads, 0, stream>>>(p);
+  return pe_host::launch_status();
+}
+
+int launch_early(const pe::StepParams& p, int dtype, int grid, cudaStream_t stream) {
+  if (dtype == PE_BF16)
+    pe::step_kernel<PE_BF16, true><<<grid, pe::kThreads, 0, stream>>>(p);
+  else
+    pe::step_kernel<PE_F32, true><<<grid, pe::kThreads, 0, stream>>>(p);
   return pe_host::launch_status();
 }
 
@@ -784,7 +933,10 @@ void bind_workspace(pe::StepParams& p, void* ws, int rows, int B) {
   char* base = static_cast<char*>(ws);
   p.sched = reinterpret_cast<uint32_t*>(base);
   p.count = reinterpret_cast<uint32_t*>(base + L.count_off);
+  p.state = reinterpret_cast<unsigned long long*>(base + L.state_off);
   p.keys = reinterpret_cast<unsigned long long*>(base + L.key_off);
+  p.rcount = reinterpret_cast<uint32_t*>(base + L.rcount_off);
+  p.amax_ws = reinterpret_cast<int32_t*>(base + L.amax_off);
 }
 
 }  // namespace
@@ -817,6 +969,7 @@ int pe_verify_greedy(const void* logits, int dtype, int64_t row_stride, int32_t 
   p.full = 0;
   p.row_bytes = row_stride * elt;
   p.logits = logits;
+  p.rows_total = B * (Kp + 1);
   p.in_tokens = in_tokens;
   p.accepted_len = accepted_len;
   p.bonus_token = bonus_token;
@@ -831,7 +984,57 @@ int pe_verify_greedy(const void* logits, int dtype, int64_t row_stride, int32_t 
   return launch(p, dtype, grid, tn, static_cast<cudaStream_t>(stream));
 }
 
-int pe_step(const pe_step_args* a, void* stream) {
+int pe_draft_readout(const void* logits, int dtype, int64_t row_stride, int32_t rows,
+                     int32_t V, const int32_t* sample_idx, int32_t n, int32_t* out_tokens,
+                     void* workspace, uint32_t* err, void* stream) {
+  const int elt = elt_size(dtype);
+  if (!elt) return PE_EDTYPE;
+  if (n < 0 || rows < 0 || V < 1 || row_stride < V) return PE_EINVAL;
+  if (n == 0) return PE_OK;
+  if (!sample_idx && n > rows) return PE_EINVAL;
+  if (!logits || !out_tokens || !workspace || !err) return PE_EINVAL;
+  if (!aligned16(logits) || !aligned16(workspace) || (row_stride * elt) % 16) return PE_EALIGN;
+  pe_host::DeviceInfo dev;
+  if (pe_host::device_info(&dev) != PE_OK) return PE_ECUDA;
+  const pe_host::Tuning tn = pe_host::tuning();
+
+  // each sampled row is a request of one verified row (K' = 0): its bonus
+  // token is the row's argmax
+  pe::StepParams p = {};
+  p.B = n;
+  p.Kp = 0;
+  p.K = 1;
+  p.V = V;
+  p.full = 0;
+  p.row_bytes = row_stride * elt;
+  p.logits = logits;
+  p.row_index = sample_idx;
+  p.rows_total = rows;
+  p.bonus_token = out_tokens;
+  p.err = err;
+  const int grid_max = grid_max_for(tn, dev);
+  plan_argmax(p, elt, n, grid_max, tn.chunk_batches);
+  p.n_units = p.n_arg_units;
+  bind_workspace(p, workspace, n, n);
+  const int grid = p.n_units < grid_max ? p.n_units : grid_max;
+  return launch(p, dtype, grid, tn, static_cast<cudaStream_t>(stream));
+}
+
+namespace {
+int step_common(const pe_step_args* a, void* stream, bool early);
+}
+
+int pe_step(const pe_step_args* a, void* stream) { return step_common(a, stream, false); }
+
+int pe_step_early_exit(const pe_step_args* a, void* stream) {
+  if (a && a->Kp > 31) return PE_EINVAL;  // one state bit per verified row
+  return step_common(a, stream, true);
+}
+
+}  // extern "C"
+
+namespace {
+int step_common(const pe_step_args* a, void* stream, bool early) {
   if (!a) return PE_EINVAL;
   const int elt = elt_size(a->logits_dtype);
   const int xelt = elt_size(a->x_dtype);
@@ -884,6 +1087,7 @@ int pe_step(const pe_step_args* a, void* stream) {
   p.nvh = (int)((long long)a->H * xelt / 16);
   p.row_bytes = a->logits_row_stride * elt;
   p.logits = a->logits;
+  p.rows_total = B * (Kp + 1);
   p.in_offsets = a->in_offsets;
   p.in_tokens = a->in_tokens;
   p.in_positions = a->in_positions;
@@ -905,14 +1109,17 @@ int pe_step(const pe_step_args* a, void* stream) {
   p.X = static_cast<uint4*>(a->X);
   p.err = a->err;
   const int rows = B * (Kp + 1);
-  const int grid_max = grid_max_for(tn, dev);
-  plan_argmax(p, elt, rows, grid_max, tn.chunk_batches);
-  p.rows_per_unit = tn.rows_per_unit;
+  // the early-exit step runs on the register-streaming kernel
+  pe_host::Tuning tk = tn;
+  if (early) tk.variant = 1;
+  const int grid_max = grid_max_for(tk, dev);
+  plan_argmax(p, elt, rows, grid_max, tk.chunk_batches);
+  p.rows_per_unit = tk.rows_per_unit;
   p.n_copy_units = (p.T + p.rows_per_unit - 1) / p.rows_per_unit;
   p.n_units = p.n_arg_units + p.n_copy_units;
   bind_workspace(p, a->workspace, rows, B);
   const int grid = p.n_units < grid_max ? p.n_units : grid_max;
-  return launch(p, a->logits_dtype, grid, tn, static_cast<cudaStream_t>(stream));
+  if (early) return launch_early(p, a->logits_dtype, grid, static_cast<cudaStream_t>(stream));
+  return launch(p, a->logits_dtype, grid, tk, static_cast<cudaStream_t>(stream));
 }
-
-}  // extern "C"
+}  // namespace

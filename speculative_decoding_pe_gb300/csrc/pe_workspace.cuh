@@ -1,13 +1,20 @@
 // Layout of the caller-provided scratch of the verify / fused-step kernels.
 //
-//   [0]   uint32 next_unit   dynamic work counter of the persistent grid
-//   [4]   uint32 ctas_done   CTAs that have left the work loop
-//   [8]   uint32 count[B]    finished argmax units per request
-//   [..]  uint64 key[rows]   running (value, column) maximum per logits row
+//   [0]   uint32 next_unit     dynamic work counter of the persistent grid
+//   [4]   uint32 ctas_done     CTAs that have left the work loop
+//   [8]   uint32 count[B]      finished argmax units per request
+//   [..]  uint64 state[B]      early exit: rows done (bits 0-31) and rows
+//                              whose argmax matched the draft (bits 32-63)
+//   [..]  uint64 key[rows]     running (value, column) maximum per logits row
+//   [..]  uint32 rcount[rows]  early exit: finished chunks per row
+//   [..]  int32  amax[rows]    early exit: argmax of each completed row
 //
-// Every field is zero between calls: the last arriving unit of a request
-// reads its keys with an exchange against 0 and clears its count; the last
-// CTA to leave clears the two scheduler words.
+// Every field is zero between calls, so one workspace serves calls of any
+// size up to the one it was sized for: the full step clears a request's keys
+// and count when its last unit arrives, the early-exit step clears completed
+// rows as they complete and everything else (partly read rows, states, row
+// results) in its last CTA; the last CTA to leave clears the two scheduler
+// words.
 #pragma once
 
 #include <stddef.h>
@@ -16,11 +23,14 @@
 namespace pe {
 
 struct WorkspaceLayout {
-  size_t count_off, key_off, bytes;
+  size_t count_off, state_off, key_off, rcount_off, amax_off, bytes;
   WorkspaceLayout(int64_t rows, int64_t B) {
     count_off = 8;
-    key_off = (count_off + 4 * (size_t)B + 7) & ~(size_t)7;
-    bytes = (key_off + 8 * (size_t)rows + 255) & ~(size_t)255;
+    state_off = (count_off + 4 * (size_t)B + 7) & ~(size_t)7;
+    key_off = state_off + 8 * (size_t)B;
+    rcount_off = key_off + 8 * (size_t)rows;
+    amax_off = rcount_off + 4 * (size_t)rows;
+    bytes = (amax_off + 4 * (size_t)rows + 255) & ~(size_t)255;
   }
 };
 

@@ -26,8 +26,12 @@ def pack(w, out, ws, err) -> _native.StepArgs:
         out=out, workspace=ws, err=err)
 
 
-def run(w, out, ws, err, stream=None):
-    _native.step_packed(pack(w, out, ws, err), stream)
+def run(w, out, ws, err, stream=None, early_exit=False):
+    args = pack(w, out, ws, err)
+    if early_exit:
+        _native.step_early_exit_packed(args, stream)
+    else:
+        _native.step_packed(args, stream)
 
 
 OUTPUT_KEYS = ("accepted_len", "bonus_token", "target_argmax", "out_offsets",

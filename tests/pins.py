@@ -61,6 +61,25 @@ def pin_argmax_numpy():
                 assert (got == ref).all(), "row stride ignored"
 
 
+def pin_draft_readout():
+    """Greedy draft tokens are numpy.argmax (first occurrence) of the rows the
+    drafter's LM head reads; an index outside the logits gives -1."""
+    g = torch.Generator().manual_seed(23)
+    for dt in (torch.float32, torch.bfloat16):
+        logits = torch.randint(-2, 3, (50, 777), generator=g).to(dt)
+        idx = torch.randint(0, 50, (64,), generator=g, dtype=torch.int32)
+        got, err = oracle.draft_readout(logits, idx)
+        ref = np.argmax(logits.float().numpy(), axis=1)[idx.numpy()]
+        assert err == 0 and (got.numpy() == ref).all()
+        got, err = oracle.draft_readout(logits)          # identity rows
+        assert err == 0 and (got.numpy() == np.argmax(logits.float().numpy(), axis=1)).all()
+        bad = torch.tensor([3, -1, 50, 7], dtype=torch.int32)
+        got, err = oracle.draft_readout(logits, bad)
+        assert err == oracle.ERR_ROW_RANGE
+        assert got[1] == -1 and got[2] == -1
+        assert got[0] == int(np.argmax(logits[3].float().numpy()))
+
+
 # ----------------------------------------------------------- acceptance (a2)
 
 def pin_accept_enumeration():
@@ -340,6 +359,7 @@ def pin_error_rules():
     assert (o3["out_tokens"] == -7).all()
 
 
-ALL_PINS = [pin_argmax_bruteforce, pin_argmax_numpy, pin_accept_enumeration,
+ALL_PINS = [pin_argmax_bruteforce, pin_argmax_numpy, pin_draft_readout,
+            pin_accept_enumeration,
             pin_planted, pin_step_invariants, pin_golden_decode,
             pin_golden_prefill, pin_error_rules]

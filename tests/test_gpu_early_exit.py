@@ -1,0 +1,103 @@
+"""Early-exit verification (pe_step_early_exit) against the CPU oracle.
+
+Every output must equal the full step's bit for bit, except target_argmax:
+rows 0..a_b of each request carry their argmax, later rows -1 (they may
+never have been read)."""
+import pytest
+import torch
+
+import pins
+from gpu_util import Guarded, assert_same, guarded_outputs, oracle_of
+from speculative_decoding_pe_gb300 import _native, build, harness
+from speculative_decoding_pe_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    build.build()
+    return _native.load()
+
+
+def run_early(w, workspace=None):
+    g = Guarded()
+    out = guarded_outputs(w, g)
+    ws = workspace if workspace is not None else _native.new_workspace(w.B * (w.Kp + 1), w.B)
+    err = _native.new_error_word()
+    harness.run(w, out, ws, err, early_exit=True)
+    torch.cuda.synchronize()
+    g.check()
+    assert int(ws.count_nonzero()) == 0, "workspace not left zeroed"
+    res = harness.to_host(out)
+    res["err"] = int(err.item())
+    return res, ws
+
+
+def check_early(w, got, ref):
+    keys = [k for k in harness.OUTPUT_KEYS if k != "target_argmax"] + ["err"]
+    assert_same(got, ref, keys=keys, what=w.spec.name + " early exit")
+    nr = w.Kp + 1
+    ta = got["target_argmax"].view(w.B, nr)
+    ra = ref["target_argmax"].view(w.B, nr)
+    for b in range(w.B):
+        a = int(ref["accepted_len"][b])
+        assert torch.equal(ta[b, :a + 1], ra[b, :a + 1]), b
+        assert (ta[b, a + 1:] == -1).all(), b
+
+
+FULL = [("tiny", 0), ("tiny", 1), ("decode_b1", 0), ("decode_b64", 0), ("prefill_b8", 0),
+        ("decode_b256", 0), ("decode_b256", 1)]
+
+
+@pytest.mark.parametrize("name,trial", FULL, ids=lambda v: str(v))
+def test_early_exit_full_size(name, trial):
+    cfg = list(wl.SPECS).index(name) + 1
+    w = wl.make_workload(name, 1000 * cfg + trial, device="cuda")
+    got, ws = run_early(w)
+    check_early(w, got, oracle_of(w))
+
+
+@pytest.mark.parametrize("spec", pins._small_specs() + [
+    wl.SPECS["decode_b256"].with_(name="all_accept", B=40, forced=tuple((b, 7) for b in range(40))),
+    wl.SPECS["decode_b256"].with_(name="none_accept", B=40, forced=tuple((b, 0) for b in range(40))),
+    wl.SPECS["decode_b256"].with_(name="ragged", B=30, V=151937, row_pad=7, H=256),
+    wl.SPECS["decode_b256"].with_(name="kp31", B=9, Kp=31, K=4, V=4099, row_pad=5, H=64,
+                                  accept_p=0.05),
+], ids=lambda s: s.name)
+def test_early_exit_variants(spec):
+    for seed in (0, 1):
+        w = wl.make_workload(spec, seed, device="cuda")
+        got, _ = run_early(w)
+        check_early(w, got, oracle_of(w))
+
+
+def test_workspace_shared_with_full_step():
+    """Early-exit and full steps alternate on one workspace; each leaves it
+    clean for the other."""
+    ws = _native.new_workspace(256 * 8, 256)
+    for i in range(6):
+        w = wl.make_workload(wl.SPECS["decode_b256"].with_(B=64 + 32 * i, V=30011, row_pad=5),
+                             300 + i, device="cuda")
+        ref = oracle_of(w)
+        if i % 2:
+            got, _ = run_early(w, ws)
+            check_early(w, got, ref)
+        else:
+            out, _, err = harness.allocate(w)
+            harness.run(w, out, ws, err)
+            torch.cuda.synchronize()
+            got = harness.to_host(out)
+            got["err"] = int(err.item())
+            assert_same(got, ref)
+        assert int(ws.count_nonzero()) == 0, i
+
+
+def test_kp_above_31_rejected():
+    w = wl.make_workload(wl.SPECS["tiny"].with_(Kp=32, K=2, B=2, V=101, row_pad=3), 0,
+                         device="cuda")
+    out, ws, err = harness.allocate(w)
+    with pytest.raises(_native.PEError):
+        harness.run(w, out, ws, err, early_exit=True)

@@ -351,3 +351,48 @@ def test_back_to_back_calls_without_sync():
         got["err"] = int(err.item())
         assert_same(got, oracle_of(w))
     assert int(ws.count_nonzero()) == 0
+
+
+# ------------------------------------------------------------ drafter readout
+
+@pytest.mark.parametrize("variant", VARIANTS, ids=VARIANT_IDS)
+@pytest.mark.parametrize("V,dtype,pad", [(151936, torch.bfloat16, 0), (201088, torch.bfloat16, 0),
+                                         (1001, torch.float32, 3), (13, torch.bfloat16, 3)])
+def test_draft_readout(V, dtype, pad, variant):
+    """Greedy t_1..t_K: the drafter's logits over all output slots, read
+    through the sample_idx the rebuild wrote; and over the sampled rows only."""
+    w = _gen(wl.SPECS["decode_b256"].with_(B=24, V=V, row_pad=pad, H=64, dtype=dtype), 3)
+    out, ws, err = harness.allocate(w)
+    harness.run(w, out, ws, err)
+    g = torch.Generator(device="cuda").manual_seed(9)
+    T = w.T
+    base = torch.randint(-3, 4, (T, V + pad), generator=g, device="cuda").to(dtype)
+    drafter = base[:, :V]                           # ties everywhere
+    sidx = out.sample_idx
+    tok = torch.full((sidx.numel(),), -9, dtype=torch.int32, device="cuda")
+    rws = _native.new_workspace(sidx.numel(), sidx.numel())
+    rerr = _native.new_error_word()
+    with tuned(**variant):
+        _native.draft_readout(drafter, tok, rws, rerr, sample_idx=sidx)
+        only = base[sidx.long()][:, :V]             # [B*K, V] rows, padded stride
+        tok2 = torch.full_like(tok, -9)
+        _native.draft_readout(only, tok2, rws, rerr)
+    torch.cuda.synchronize()
+    ref, e = oracle.draft_readout(drafter.cpu(), sidx.cpu())
+    assert e == 0 and int(rerr.item()) == 0
+    assert torch.equal(tok.cpu(), ref) and torch.equal(tok2.cpu(), ref)
+    assert int(rws.count_nonzero()) == 0
+
+
+def test_draft_readout_bad_rows():
+    logits = torch.randn(40, 1000, device="cuda")
+    idx = torch.tensor([5, -1, 40, 39, 2 ** 30], dtype=torch.int32, device="cuda")
+    tok = torch.full((5,), -9, dtype=torch.int32, device="cuda")
+    ws = _native.new_workspace(5, 5)
+    err = _native.new_error_word()
+    _native.draft_readout(logits, tok, ws, err, sample_idx=idx)
+    torch.cuda.synchronize()
+    ref, e = oracle.draft_readout(logits.cpu(), idx.cpu())
+    assert e == oracle.ERR_ROW_RANGE == int(err.item())
+    assert torch.equal(tok.cpu(), ref)
+    assert int(ws.count_nonzero()) == 0

@@ -58,6 +58,8 @@ MUTANTS = {
     "emb_of_wrong_row": ("memcpy(dst, (const char*)emb + (size_t)tok * half, half);",
                          "memcpy(dst, (const char*)emb + (size_t)(tok ^ 1) * half, half);"),
     "bf16_low_half": ("bits = ((uint32_t)h) << 16;", "bits = ((uint32_t)h);"),
+    "readout_ignores_sample_idx": ("int32_t r = sample_idx ? sample_idx[i] : i;",
+                                   "int32_t r = i;"),
 }
 
 
