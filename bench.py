@@ -99,17 +99,18 @@ def rank_seed(workload: str, rank: int) -> int:
 
 # ------------------------------------------------------------ byte counts
 
-def algorithmic_bytes(spec: wl.WorkloadSpec, R: int) -> dict:
+def algorithmic_bytes(spec: wl.WorkloadSpec, R: int, logits_rows: int | None = None) -> dict:
     """Bytes one step must move at minimum (each byte counted once).
 
     logits: every row read once; hidden: every target row read once;
     emb: one table row per verified / prompt slot plus the MASK row (the
     repeated MASK-row reads hit L2); X: written once; metadata: 18 bytes per
     output slot (token, position, two masks, slot id) plus the per-row and
-    per-request integers."""
+    per-request integers.  With early exit, ``logits_rows`` is the number of
+    rows a greedy verifier must read (rows 0..a_b of each request)."""
     B, Kp, K, V, H = spec.B, spec.Kp, spec.K, spec.V, spec.H
     elt = torch.tensor([], dtype=spec.dtype).element_size()
-    Rl = B * (Kp + 1)
+    Rl = B * (Kp + 1) if logits_rows is None else logits_rows
     T = R + B * (K - 1)
     parts = {
         "logits": Rl * V * elt,
@@ -321,8 +322,10 @@ def run_ours(args):
     flush = torch.empty(2 * l2, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
 
+    run_step = _native.step_early_exit_packed if args.early_exit else _native.step_packed
+
     def step():
-        _native.step_packed(packed, stream)
+        run_step(packed, stream)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -353,14 +356,18 @@ def run_ours(args):
     T = w.T
     value, mean_ms_max, rows_all = aggregate(float(T), mean_ms, world, device)
 
-    bytes_ = algorithmic_bytes(spec, w.R)
+    needed = None
+    if args.early_exit:  # rows 0..a_b of each request, a_b as planted
+        needed = int((w.planted_accept.long() + 1).sum())
+    bytes_ = algorithmic_bytes(spec, w.R, needed)
     peak, peak_kind = measured_peak()
     achieved = bytes_["total"] / (mean_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
                 "peak_source": peak_kind, "algorithmic_bytes_per_launch": bytes_["total"],
-                "kernel": "pe::step_kernel<bf16>" if spec.dtype == torch.bfloat16
-                else "pe::step_kernel<f32>"}
+                "kernel": "pe::step_kernel<%s, early_exit=%s>" % (
+                    "bf16" if spec.dtype == torch.bfloat16 else "f32",
+                    "true" if args.early_exit else "false")}
 
     e2e = measure_e2e(w, out, ws, err, packed, stream, device, args) if args.e2e else None
     if e2e is not None:
@@ -368,6 +375,8 @@ def run_ours(args):
         e2e = {"value": rows_all / (e2e_ms / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
                "ms_per_step": e2e_ms}
+
+    graph = measure_graph(spec, args, device, run_step) if args.graph else None
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_baseline:
@@ -380,6 +389,8 @@ def run_ours(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": str(spec.dtype).replace("torch.", ""), "data": "synthetic",
             "config": config_of(spec, {"T_per_rank": T, "R_per_rank": w.R,
+                                       "early_exit": bool(args.early_exit),
+                                       "logits_rows_needed": needed,
                                        "median_us": statistics.median(step_ms) * 1e3,
                                        "min_us": min(step_ms) * 1e3,
                                        "tuning": _native.get_tuning()}),
@@ -391,6 +402,8 @@ def run_ours(args):
             "gpu_launches": args.steps,
             "clocks": clocks,
         }
+        if graph is not None:
+            line["graph"] = graph
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
@@ -418,10 +431,12 @@ def measure_e2e(w, out, ws, err, packed, stream, device, args):
     d2h = sum(r.numel() * r.element_size() for r in res_host)
     n = max(3, min(args.steps, args.e2e_steps))
 
+    run_step = _native.step_early_exit_packed if args.early_exit else _native.step_packed
+
     def one():
         for d, h in host:
             d.copy_(h, non_blocking=True)
-        _native.step_packed(packed, stream)
+        run_step(packed, stream)
         for d, h in zip(res_dev, res_host):
             h.copy_(d, non_blocking=True)
 
@@ -435,6 +450,43 @@ def measure_e2e(w, out, ws, err, packed, stream, device, args):
     e1.record(stream)
     torch.cuda.synchronize(device)
     return {"ms": e0.elapsed_time(e1) / n, "h2d": h2d, "d2h": d2h}
+
+
+def measure_graph(spec, args, device, run_step):
+    """N steps, each over its own input set, captured in one CUDA graph and
+    replayed; events around whole replays.  No L2 flush: the N input sets
+    are distinct (for the large workloads they are far larger than L2)."""
+    from speculative_decoding_pe_gb300 import _native, harness
+    n = args.graph
+    ws_list = [wl.make_workload(spec, 9000 + i, device=device) for i in range(n)]
+    ws = _native.new_workspace(spec.B * (spec.Kp + 1), spec.B, device)
+    bufs = [harness.allocate(w, device) for w in ws_list]
+    packed = [harness.pack(w, out, ws, err) for w, (out, _, err) in zip(ws_list, bufs)]
+    s = torch.cuda.Stream(device)
+    s.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(s):
+        for a in packed:
+            run_step(a, s)
+    torch.cuda.synchronize(device)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for a in packed:
+            run_step(a, torch.cuda.current_stream(device))
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize(device)
+    reps = max(3, args.steps // n)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream(device)
+    e0.record(cur)
+    for _ in range(reps):
+        g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize(device)
+    us = e0.elapsed_time(e1) * 1e3 / (reps * n)
+    return {"steps_per_graph": n, "replays": reps, "us_per_step": us,
+            "value": float(ws_list[0].T) / (us * 1e-6), "unit": UNIT,
+            "inputs": "%d distinct input sets, no flush between steps" % n}
 
 
 def measure_cpu_baseline(w, budget_s: float):
@@ -458,6 +510,11 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(wl.SPECS), default="decode_b256")
     ap.add_argument("--tuning", default="", help="JSON launch-shape knobs")
+    ap.add_argument("--graph", type=int, default=0,
+                    help="also time N steps captured in one CUDA graph")
+    ap.add_argument("--early-exit", action="store_true",
+                    help="time pe_step_early_exit (rows after each request's first "
+                         "mismatch are not read)")
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")

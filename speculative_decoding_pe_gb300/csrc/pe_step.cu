@@ -90,7 +90,8 @@ struct SharedState {
   int unit;
   int last;
   int first;
-  int skip;
+  int skip2[2];  // early exit: unit is moot
+  int next2[2];  // early exit: next unit after a moot one
   int verdict[2];
   int amax[PE_MAX_KP + 1];
   int tok[PE_MAX_KP + 1];
@@ -439,15 +440,7 @@ __device__ __forceinline__ void argmax_unit_early(const StepParams& p, SharedSta
   const int rem = u - j * per_row;
   const int b = rem / p.C;
   const int c = rem - b * p.C;
-  const int r = b * (p.Kp + 1) + j;
-  if (tid == 0) {  // a mismatch already known at an earlier row makes this row moot
-    const unsigned long long st = __ldcg(p.state + b);
-    const unsigned done = (unsigned)st;
-    const unsigned match = (unsigned)(st >> 32);
-    sh.skip = (done & ~match & ((1u << j) - 1u)) != 0u;
-  }
-  __syncthreads();
-  if (sh.skip) return;
+  const int r = b * (p.Kp + 1) + j;  // (moot units were skipped by the caller)
   const char* rowp = logits_row(p, r);
   const int v_lo = c * p.chunk_vecs;
   const int v_hi = min(v_lo + p.chunk_vecs, p.nvec);
@@ -611,9 +604,34 @@ __global__ void __launch_bounds__(kThreads, 3) step_kernel(const StepParams p) {
   // The first unit of each CTA is its own index; later units come from the
   // counter, which therefore hands out gridDim.x + 0, 1, 2, ...
   int u = blockIdx.x;
+  int par = 0;
   while (u < p.n_units) {
     unsigned next = 0;
     if (threadIdx.x == 0) next = gridDim.x + atomicAdd(p.sched, 1u);  // prefetch
+    if (EARLY && u < p.n_arg_units && u >= p.B * p.C) {
+      // rows after row 0: moot once a mismatch is known at an earlier row.
+      // The state load and the next-unit fetch are in flight together; a
+      // moot unit costs one round trip and one barrier.
+      if (threadIdx.x == 0) {
+        const int per_row = p.B * p.C;
+        const int j = u / per_row;
+        const int b = (u - j * per_row) / p.C;
+        const unsigned long long st = __ldcg(p.state + b);
+        const unsigned done = (unsigned)st;
+        const unsigned match = (unsigned)(st >> 32);
+        const int moot = (done & ~match & ((1u << j) - 1u)) != 0u;
+        sh.skip2[par] = moot;
+        if (moot) sh.next2[par] = (int)next;
+      }
+      __syncthreads();
+      const int moot = sh.skip2[par];
+      const int nu = sh.next2[par];
+      par ^= 1;  // two slots: no thread is ever two barriers behind
+      if (moot) {
+        u = nu;
+        continue;
+      }
+    }
     if (u < p.n_arg_units) {
       if (EARLY)
         argmax_unit_early<DT>(p, sh, u);
@@ -845,7 +863,11 @@ using pe_host::aligned16;
 using pe_host::elt_size;
 
 // Argmax chunking and grid size for `rows` logits rows of `V` elements.
-void plan_argmax(pe::StepParams& p, int elt, int rows, int grid_max, int batches) {
+// want_rows: the rows over which ~one unit per CTA is wanted (all rows, or
+// for early exit half a row wave, so that each wave gives ~2 units per CTA).
+void plan_argmax(pe::StepParams& p, int elt, int rows, int grid_max, int batches,
+                 int want_rows = 0) {
+  if (want_rows <= 0) want_rows = rows;
   const int epv = 16 / elt;
   p.Rl = rows;
   p.nvec = p.V / epv;
@@ -856,7 +878,7 @@ void plan_argmax(pe::StepParams& p, int elt, int rows, int grid_max, int batches
   } else {
     const long long cap = (long long)batches * pe::kBatchVecs;
     int c_min = (int)((p.nvec + cap - 1) / cap);
-    int c_want = (grid_max + rows - 1) / rows;  // at least ~one unit per CTA
+    int c_want = (grid_max + want_rows - 1) / want_rows;  // at least ~one unit per CTA
     int c_max = (p.nvec + pe::kThreads - 1) / pe::kThreads;
     int C = c_min > c_want ? c_min : c_want;
     if (C > c_max) C = c_max;
