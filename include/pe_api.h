@@ -225,7 +225,9 @@ int pe_step(const pe_step_args* args /* host */, void* stream);
  * target_argmax, which holds each request's rows 0..a_b and -1 for the rows
  * after a_b.  Same arguments and workspace as pe_step; Kp <= 31 (one bit per
  * verified row), else PE_EINVAL.  Always runs the register-streaming kernel
- * (pe_tuning.variant does not apply). */
+ * (pe_tuning.variant does not apply).  It pays off when many requests share
+ * the step (their rows interleave); with one or a few requests the rows of a
+ * request serialise and the full-read pe_step is faster. */
 int pe_step_early_exit(const pe_step_args* args /* host */, void* stream);
 
 /* pe_step for callers that cannot allocate device memory at all, not even
