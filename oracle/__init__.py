@@ -40,7 +40,7 @@ def compile_source(src: str, out: str) -> str:
     """gcc -O2 one C file (plain, no vector intrinsics) into a shared library."""
     tmp = out + ".tmp%d" % os.getpid()
     cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-Wall", "-Werror",
-           "-I", _HERE, "-o", tmp, src]
+           "-I", _HERE, "-o", tmp, src, "-lm"]
     subprocess.run(cmd, check=True)
     os.replace(tmp, out)
     return out
@@ -83,6 +83,10 @@ def _load():
             lib.oracle_verify_greedy.argtypes = [P, c_int, i64, i32, i32, i32,
                                                  P, P, P, P]
             lib.oracle_draft_readout.argtypes = [P, c_int, i64, i32, i32, P, i32, P, P]
+            lib.oracle_philox4x32_10.argtypes = [P, P, P]
+            lib.oracle_philox4x32_10.restype = None
+            lib.oracle_verify_sampled.argtypes = [P, P, c_int, i64, i64, i32, i32, i32, P, P,
+                                                  ctypes.c_float, ctypes.c_uint64, P, P]
             lib.oracle_build_draft_batch.argtypes = (
                 [i32, i32, i32, i32, P, P, P, P, P, P, i32, i32] + [P] * 9)
             lib.oracle_assemble_draft_inputs.argtypes = (
@@ -91,7 +95,7 @@ def _load():
                 [c_int, c_int, i32, i32, i32, i32, i32, i32, P, i64, P, P, P, P,
                  i32, i32, P, P, P] + [P] * 13)
             for fn in (lib.oracle_argmax_rows, lib.oracle_verify_greedy,
-                       lib.oracle_draft_readout,
+                       lib.oracle_draft_readout, lib.oracle_verify_sampled,
                        lib.oracle_build_draft_batch,
                        lib.oracle_assemble_draft_inputs, lib.oracle_step):
                 fn.restype = ctypes.c_int
@@ -152,6 +156,36 @@ def draft_readout(logits, sample_idx=None, n=None):
                                     logits.shape[0], logits.shape[1], _ptr(idx), n,
                                     _ptr(out), ctypes.byref(err)), "draft_readout")
     return out, err.value
+
+
+def philox4x32_10(counter, key):
+    """Philox4x32-10 of a 4-word counter under a 2-word key."""
+    lib = _load()
+    c = (ctypes.c_uint32 * 4)(*counter)
+    k = (ctypes.c_uint32 * 2)(*key)
+    o = (ctypes.c_uint32 * 4)()
+    lib.oracle_philox4x32_10(c, k, o)
+    return list(o)
+
+
+def verify_sampled(target_logits, draft_logits, B, Kp, tokens, u_accept, temperature,
+                   seed):
+    """Rejection-sampling verification; returns (accepted_len[B], bonus[B])."""
+    lib = _load()
+    t = target_logits.detach().cpu()
+    assert t.dim() == 2 and t.stride(1) == 1
+    d = draft_logits.detach().cpu() if draft_logits is not None else None
+    if d is not None:
+        assert d.dtype == t.dtype and d.stride(1) == 1
+    tok = _i32(tokens)
+    u = u_accept.detach().to("cpu", torch.float32).contiguous() if u_accept is not None else None
+    acc = torch.empty(B, dtype=torch.int32)
+    bon = torch.empty(B, dtype=torch.int32)
+    _check(lib.oracle_verify_sampled(
+        _ptr(t), _ptr(d), _dt(t), t.stride(0), d.stride(0) if d is not None else 0, B, Kp,
+        t.shape[1], _ptr(tok), _ptr(u), float(temperature), int(seed), _ptr(acc), _ptr(bon)),
+        "verify_sampled")
+    return acc, bon
 
 
 def verify_greedy(logits, B, Kp, V, tokens):

@@ -30,6 +30,7 @@
  */
 #include "pe_oracle.h"
 
+#include <math.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -132,6 +133,151 @@ int oracle_verify_greedy(const void* logits, int dtype, int64_t row_stride,
     bonus_token[b] = amax[first + a]; /* target token at the first mismatch */
   }
   if (!target_argmax) free(amax);
+  return 0;
+}
+
+/* ---- rejection-sampling verification ----------------------------------- */
+/* "并行草稿机制解析：从P-EAGLE到DSpark的投机采样加速" §1.2: the target checks the
+   drafts one by one against its own distribution, accepts when they agree
+   well enough and otherwise replaces from that position with its own output,
+   so that the result has exactly the target's distribution.  Read as the
+   standard rule: accept with probability min(1, p/q); on rejection draw from
+   the normalised max(0, p - q); after all acceptances draw from p. */
+
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2],
+                          uint32_t out[4]) {
+  uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+  uint32_t k0 = key[0], k1 = key[1];
+  int r;
+  for (r = 0; r < 10; ++r) {
+    uint64_t p0, p1;
+    uint32_t n0, n2;
+    if (r > 0) { /* key schedule: Weyl increments */
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    p0 = (uint64_t)0xD2511F53u * c0;
+    p1 = (uint64_t)0xCD9E8D57u * c2;
+    n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+    n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+    c1 = (uint32_t)p1;
+    c3 = (uint32_t)p0;
+    c0 = n0;
+    c2 = n2;
+  }
+  out[0] = c0;
+  out[1] = c1;
+  out[2] = c2;
+  out[3] = c3;
+}
+
+/* Gumbel noise for element i of draw `stream` */
+static double gumbel(uint64_t seed, uint32_t stream, int32_t i) {
+  uint32_t ctr[4], key[2], w[4];
+  double u;
+  ctr[0] = (uint32_t)i >> 2;
+  ctr[1] = stream;
+  ctr[2] = 0;
+  ctr[3] = 0;
+  key[0] = (uint32_t)seed;
+  key[1] = (uint32_t)(seed >> 32);
+  oracle_philox4x32_10(ctr, key, w);
+  u = ((double)(w[i & 3] >> 8) + 0.5) / 16777216.0; /* 24 bits: exact in fp32 */
+  return -log(-log(u));
+}
+
+/* probability of column x under softmax(row / temperature) */
+static double softmax_at(const void* logits, int dtype, int64_t base, int32_t V,
+                         double inv_t, int32_t x) {
+  double m = -INFINITY, s = 0.0;
+  int32_t v;
+  for (v = 0; v < V; ++v) {
+    double z = load_elem(logits, dtype, base + v) * inv_t;
+    if (z > m) m = z;
+  }
+  for (v = 0; v < V; ++v) s += exp(load_elem(logits, dtype, base + v) * inv_t - m);
+  return exp(load_elem(logits, dtype, base + x) * inv_t - m) / s;
+}
+
+int oracle_verify_sampled(const void* target_logits, const void* draft_logits,
+                          int dtype, int64_t target_stride,
+                          int64_t draft_stride, int32_t B, int32_t Kp,
+                          int32_t V, const int32_t* tokens,
+                          const float* u_accept, float temperature,
+                          uint64_t seed, int32_t* accepted_len,
+                          int32_t* bonus_token) {
+  int32_t b, j, v;
+  double inv_t;
+  if (B < 0 || Kp < 0 || V < 1 || !(temperature > 0.0f)) return -1;
+  if (B == 0) return 0;
+  if (!target_logits || !accepted_len || !bonus_token) return -1;
+  if (Kp > 0 && (!draft_logits || !tokens || !u_accept)) return -1;
+  inv_t = 1.0 / (double)temperature;
+  for (b = 0; b < B; ++b) {
+    int32_t a = Kp, best = 0;
+    double best_s = -INFINITY;
+    int64_t trow, drow;
+    for (j = 0; j < Kp; ++j) {
+      int32_t x = tokens[(int64_t)b * (Kp + 1) + j + 1];
+      double px, qx;
+      trow = ((int64_t)b * (Kp + 1) + j) * target_stride;
+      drow = ((int64_t)b * Kp + j) * draft_stride;
+      if (x < 0 || x >= V) {
+        a = j;
+        break;
+      }
+      px = softmax_at(target_logits, dtype, trow, V, inv_t, x);
+      qx = softmax_at(draft_logits, dtype, drow, V, inv_t, x);
+      if (!((double)u_accept[(int64_t)b * Kp + j] * qx < px)) {
+        a = j;
+        break;
+      }
+    }
+    trow = ((int64_t)b * (Kp + 1) + a) * target_stride;
+    if (a < Kp) { /* draw from max(0, p - q) */
+      double mt = -INFINITY, md = -INFINITY, st = 0.0, sd = 0.0;
+      int any = 0;
+      drow = ((int64_t)b * Kp + a) * draft_stride;
+      for (v = 0; v < V; ++v) {
+        double zt = load_elem(target_logits, dtype, trow + v) * inv_t;
+        double zd = load_elem(draft_logits, dtype, drow + v) * inv_t;
+        if (zt > mt) mt = zt;
+        if (zd > md) md = zd;
+      }
+      for (v = 0; v < V; ++v) {
+        st += exp(load_elem(target_logits, dtype, trow + v) * inv_t - mt);
+        sd += exp(load_elem(draft_logits, dtype, drow + v) * inv_t - md);
+      }
+      for (v = 0; v < V; ++v) {
+        double pv = exp(load_elem(target_logits, dtype, trow + v) * inv_t - mt) / st;
+        double qv = exp(load_elem(draft_logits, dtype, drow + v) * inv_t - md) / sd;
+        if (pv - qv > 0.0) {
+          double sc = log(pv - qv) + gumbel(seed, (uint32_t)b, v);
+          if (!any || sc > best_s) {
+            best_s = sc;
+            best = v;
+          }
+          any = 1;
+        }
+      }
+      if (any) {
+        accepted_len[b] = a;
+        bonus_token[b] = best;
+        continue;
+      }
+      /* p == q: the residual is empty, draw from p */
+    }
+    for (v = 0; v < V; ++v) { /* draw from softmax(row / temperature) */
+      double sc = load_elem(target_logits, dtype, trow + v) * inv_t +
+                  gumbel(seed, (uint32_t)b, v);
+      if (v == 0 || sc > best_s) {
+        best_s = sc;
+        best = v;
+      }
+    }
+    accepted_len[b] = a;
+    bonus_token[b] = best;
+  }
   return 0;
 }
 

@@ -48,6 +48,31 @@ int oracle_verify_greedy(const void* logits, int dtype, int64_t row_stride,
                          const int32_t* tokens, int32_t* accepted_len,
                          int32_t* bonus_token, int32_t* target_argmax);
 
+/* Philox4x32-10 counter-based generator (Salmon, Moraes, Dror, Shaw,
+ * "Parallel Random Numbers: As Easy as 1, 2, 3", SC'11): out = the counter
+ * after ten rounds under the key. */
+void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2],
+                          uint32_t out[4]);
+
+/* Rejection-sampling verification (the acceptance rule of speculative
+ * sampling).  For request b and draft j (0 <= j < Kp), with
+ * p = softmax(target row b(Kp+1)+j / temperature), q = softmax(draft row
+ * b*Kp+j / temperature) and x = tokens[b(Kp+1)+j+1]: the draft is accepted
+ * when u_accept[b*Kp+j] * q(x) < p(x).  At the first rejection a_b = j and
+ * the bonus is drawn from max(0, p - q) (from p when that is all zero);
+ * when every draft is accepted a_b = Kp and the bonus is drawn from
+ * softmax(target row b(Kp+1)+Kp / temperature).  Draws use the Gumbel-max
+ * rule with noise -log(-log(U)), U = ((w >> 8) + 0.5) / 2^24, w = word (i mod 4)
+ * of Philox4x32-10(counter = (i / 4, b, 0, 0), key = (seed lo, seed hi)).
+ * A draft token outside [0, V) is rejected. */
+int oracle_verify_sampled(const void* target_logits, const void* draft_logits,
+                          int dtype, int64_t target_stride,
+                          int64_t draft_stride, int32_t B, int32_t Kp,
+                          int32_t V, const int32_t* tokens,
+                          const float* u_accept, float temperature,
+                          uint64_t seed, int32_t* accepted_len,
+                          int32_t* bonus_token);
+
 /* Draft-batch rebuild.  in_offsets[B+1] (NULL: fixed segments of Kp+1
  * rows); accepted_len[B] (NULL: all zero).  Outputs sized from
  * R = in_offsets[B] and T = R + B*(K-1).  sample_idx[B*K] may be NULL. */

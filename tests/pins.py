@@ -120,6 +120,101 @@ def pin_planted(spec_names=("tiny",), seeds=(0, 1, 2, 3)):
             assert torch.equal(bon[known], w.planted_bonus[known]), (name, seed)
 
 
+# ------------------------------------------------ rejection sampling (next row)
+
+def pin_philox_known_answers():
+    """Philox4x32-10 reproduces the known-answer vectors published with the
+    generator (Salmon et al., SC'11; Random123 distribution)."""
+    kat = [((0, 0, 0, 0), (0, 0), (0x6627e8d5, 0xe169c58d, 0xbc57ac4c, 0x9b00dbd8)),
+           ((0xffffffff,) * 4, (0xffffffff,) * 2,
+            (0x408f276d, 0x41c83b0e, 0xa20bc7c6, 0x6d5451fd)),
+           ((0x243f6a88, 0x85a308d3, 0x13198a2e, 0x03707344), (0xa4093822, 0x299f31d0),
+            (0xd16cfe09, 0x94fdcceb, 0x5001e420, 0x24126ea1))]
+    for ctr, key, want in kat:
+        assert tuple(oracle.philox4x32_10(ctr, key)) == want
+
+
+def _sharp_case(B=40, Kp=5, V=61, seed=3):
+    """Target rows with distinct integer logits and draft rows one-hot at the
+    draft token; planted acceptance as in the synthetic workloads."""
+    g = torch.Generator().manual_seed(seed)
+    t = torch.stack([torch.randperm(V, generator=g).float() for _ in range(B * (Kp + 1))])
+    amax = t.argmax(1)
+    tokens = torch.randint(0, V, (B * (Kp + 1),), generator=g, dtype=torch.int32)
+    for b in range(B):
+        a = int(torch.randint(0, Kp + 1, (), generator=g))
+        for j in range(Kp):
+            row = b * (Kp + 1) + j
+            if j < a:
+                tokens[row + 1] = amax[row]
+            elif j == a and int(tokens[row + 1]) == int(amax[row]):
+                tokens[row + 1] = (amax[row] + 1) % V
+    d = torch.full((B * Kp, V), -50.0)
+    for b in range(B):
+        for j in range(Kp):
+            d[b * Kp + j, int(tokens[b * (Kp + 1) + j + 1])] = 50.0
+    u = torch.rand(B * Kp, generator=g) * 0.999 + 0.0005
+    return t, d, tokens, u
+
+
+def pin_sampled_cold_is_greedy():
+    """At a cold temperature with one-hot drafts, speculative sampling must
+    accept exactly the drafts greedy verification accepts and draw the
+    greedy bonus (the target's distribution is then one-hot)."""
+    B, Kp = 40, 5
+    t, d, tokens, u = _sharp_case(B, Kp)
+    acc, bon = oracle.verify_sampled(t, d, B, Kp, tokens, u, 0.01, 11)
+    gacc, gbon, _ = oracle.verify_greedy(t, B, Kp, t.shape[1], tokens)
+    assert torch.equal(acc, gacc) and torch.equal(bon, gbon)
+    assert 0 < int((acc == Kp).sum()) < B and int((acc < Kp).sum()) > 0
+
+
+def pin_sampled_same_distribution_accepts_all():
+    """When the drafter's distribution equals the target's, every draft is
+    accepted (u * q(x) < p(x) for every u in [0, 1))."""
+    g = torch.Generator().manual_seed(5)
+    B, Kp, V = 30, 4, 97
+    t = torch.randn(B * (Kp + 1), V, generator=g)
+    d = torch.stack([t[b * (Kp + 1) + j] for b in range(B) for j in range(Kp)])
+    tokens = torch.randint(0, V, (B * (Kp + 1),), generator=g, dtype=torch.int32)
+    u = torch.rand(B * Kp, generator=g)
+    acc, _ = oracle.verify_sampled(t, d, B, Kp, tokens, u, 0.7, 3)
+    assert (acc == Kp).all()
+
+
+def _chi2(counts, probs):
+    n = counts.sum()
+    exp = probs * n
+    return float(((counts - exp) ** 2 / exp).sum())
+
+
+def pin_sampled_preserves_target_distribution():
+    """The guarantee of speculative sampling: whatever the drafter proposes,
+    the first emitted token is distributed as the target's p_0, and after an
+    accepted draft the bonus is distributed as p_1 (chi-square, 3 degrees of
+    freedom, 99.9 % quantile 16.27, over 40000 draws)."""
+    rng = np.random.default_rng(17)
+    N, V = 40000, 4
+    p0 = np.array([0.1, 0.2, 0.3, 0.4])
+    p1 = np.array([0.4, 0.3, 0.2, 0.1])
+    q0 = np.array([0.4, 0.4, 0.1, 0.1])
+    t = torch.tensor(np.log(np.stack([p0, p1] * N)), dtype=torch.float32)
+    d = torch.tensor(np.log(np.stack([q0] * N)), dtype=torch.float32)
+    x = rng.choice(V, size=N, p=q0)
+    tokens = torch.zeros(2 * N, dtype=torch.int32)
+    tokens[1::2] = torch.tensor(x, dtype=torch.int32)
+    u = torch.tensor(rng.random(N), dtype=torch.float32)
+    acc, bon = oracle.verify_sampled(t, d, N, 1, tokens, u, 1.0, 2024)
+    acc, bon = acc.numpy(), bon.numpy()
+    first = np.where(acc >= 1, x, bon)
+    assert _chi2(np.bincount(first, minlength=V), p0) < 16.27
+    after = bon[acc == 1]
+    assert _chi2(np.bincount(after, minlength=V), p1) < 16.27
+    # a plain draw (no drafts) is distributed as p_0 too
+    acc0, bon0 = oracle.verify_sampled(t[0::2].contiguous(), None, N, 0, None, None, 1.0, 99)
+    assert _chi2(np.bincount(bon0.numpy(), minlength=V), p0) < 16.27
+
+
 # -------------------------------------------------- rebuild invariants (a3-a5)
 
 def check_rebuild_invariants(w, o):
@@ -360,6 +455,8 @@ def pin_error_rules():
 
 
 ALL_PINS = [pin_argmax_bruteforce, pin_argmax_numpy, pin_draft_readout,
-            pin_accept_enumeration,
+            pin_philox_known_answers, pin_sampled_cold_is_greedy,
+            pin_sampled_same_distribution_accepts_all,
+            pin_sampled_preserves_target_distribution, pin_accept_enumeration,
             pin_planted, pin_step_invariants, pin_golden_decode,
             pin_golden_prefill, pin_error_rules]

@@ -60,6 +60,12 @@ MUTANTS = {
     "bf16_low_half": ("bits = ((uint32_t)h) << 16;", "bits = ((uint32_t)h);"),
     "readout_ignores_sample_idx": ("int32_t r = sample_idx ? sample_idx[i] : i;",
                                    "int32_t r = i;"),
+    "sampled_accept_ignores_q": ("if (!((double)u_accept[(int64_t)b * Kp + j] * qx < px)) {",
+                                 "if (!((double)u_accept[(int64_t)b * Kp + j] < px + 0.0 * qx)) {"),
+    "sampled_residual_is_p": ("if (pv - qv > 0.0) {\n          double sc = log(pv - qv)",
+                              "if (pv > 0.0 * qv) {\n          double sc = log(pv)"),
+    "gumbel_sign_flipped": ("return -log(-log(u));", "return log(-log(u));"),
+    "philox_nine_rounds": ("for (r = 0; r < 10; ++r) {", "for (r = 0; r < 9; ++r) {"),
 }
 
 
