@@ -12,6 +12,10 @@
  *  [P2] "P-EAGLE: Parallel Speculative Decoding in vLLM" -- Step 2: Parallel
  *       Drafting; Fused Triton Kernel; Hidden State Management; KV Cache and
  *       CUDA Graphs.
+ *  [P3] "并行草稿机制解析：从P-EAGLE到DSpark的投机采样加速" -- §1.2 (the
+ *       target checks the drafts against its own distribution, accepts the
+ *       ones that agree and replaces from the first disagreement, keeping
+ *       its own output distribution).
  *
  * Notation.  Request b in [0,B).  Its target (verification) segment holds
  * n_b rows starting at input offset io_b; decode has n_b = K'+1 (the last
@@ -33,7 +37,8 @@
  *    to) and writes the defined value stated for that case.
  *  - Integer outputs are exact.  Floating point only enters the argmax:
  *    values are compared numerically (-0.0 == +0.0), the lowest column wins
- *    ties; logits must not hold NaN.
+ *    ties; logits must not hold NaN.  (pe_verify_sampled is the exception:
+ *    it decides in fp32 arithmetic, see there.)
  *  - Element types: PE_F32 (4 bytes) or PE_BF16 (2 bytes).  Embedding table,
  *    target hidden rows, h_shared and X share one element type.
  *  - Alignment: logits base, emb, target_hidden, h_shared and X must be
@@ -117,6 +122,49 @@ int pe_draft_readout(const void* logits, int dtype, int64_t row_stride,
                      int32_t rows, int32_t V, const int32_t* sample_idx,
                      int32_t n, int32_t* out_tokens, void* workspace,
                      uint32_t* err, void* stream);
+
+/* Bytes of scratch that pe_verify_sampled needs for B requests of depth Kp
+ * (any V).  Allocated once, zero-filled; every call leaves it zeroed again,
+ * so it serves every later call with B and Kp up to those. */
+size_t pe_workspace_bytes_sampled(int32_t B, int32_t Kp);
+
+/* Rejection-sampling verification [P3 §1.2], read as the acceptance rule of
+ * speculative sampling, for callers that sample rather than take argmax.
+ * With T = temperature, for request b and draft j < Kp:
+ *   p_j = softmax(target row b(Kp+1)+j / T),  q_j = softmax(draft row
+ *   b*Kp+j / T),  x = in_tokens[b(Kp+1)+j+1]  (the draft d_{j+1});
+ *   draft j is accepted when u_accept[b*Kp+j] * q_j(x) < p_j(x)
+ *   (probability min(1, p/q) for u uniform in [0,1)); a token outside
+ *   [0,V) is rejected.
+ *   accepted_len[b] = a_b = the first rejected j, or Kp.
+ *   bonus_token[b] = a draw from max(0, p_a - q_a) normalised when a_b < Kp
+ *   (from p_a when that residual is zero everywhere), from p_Kp (target
+ *   row b(Kp+1)+Kp) when a_b = Kp.
+ * Draws are Gumbel-max: the column maximising s(v) + G_b(v), s(v) = log of
+ * the (unnormalised) weight of column v, G_b(v) = -log(-log(U)),
+ * U = ((w >> 8) + 0.5) / 2^24 and w = word (v mod 4) of Philox4x32-10
+ * (Salmon et al., SC'11) at counter (v/4, b, 0, 0) under the key (low,
+ * high word of `seed`).  Only the accept/reject coins come from the caller.
+ *  target_logits [B*(Kp+1), V], row stride target_stride elements.
+ *  draft_logits  [B*Kp, V], row stride draft_stride (the drafter's logits
+ *                at the drafted positions); NULL allowed when Kp == 0.
+ *  in_tokens     [B*(Kp+1)] int32 as for pe_verify_greedy; u_accept
+ *                [B*Kp] fp32 in [0,1).  Both may be NULL when Kp == 0.
+ *  temperature   > 0 (PE_EINVAL otherwise); logits must be finite.
+ *  workspace     pe_workspace_bytes_sampled(B, Kp) bytes, zeroed.
+ *  err           device error word (no bits are defined for this call).
+ * Arithmetic is fp32 (exp and log of CUDA's fast intrinsics for the
+ * probabilities, logf for the noise): accept decisions and draws agree with
+ * an exact evaluation except where p(x) - u q(x), or the gap between the
+ * two best Gumbel scores, is within rounding of zero.  Two kernel launches;
+ * B == 0 enqueues nothing. */
+int pe_verify_sampled(const void* target_logits, const void* draft_logits,
+                      int dtype, int64_t target_stride, int64_t draft_stride,
+                      int32_t B, int32_t Kp, int32_t V,
+                      const int32_t* in_tokens, const float* u_accept,
+                      float temperature, uint64_t seed, int32_t* accepted_len,
+                      int32_t* bonus_token, void* workspace, uint32_t* err,
+                      void* stream);
 
 /* Draft-batch rebuild [P2 Fused Triton Kernel; KV Cache and CUDA Graphs].
  * For request b with bonus slot s_b = n_b-1-Kp+a_b and slot k of its output

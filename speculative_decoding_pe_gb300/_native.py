@@ -30,6 +30,7 @@ MAX_KP, MAX_K = 255, 256
 
 # every function the C header declares
 EXPORTS = ("pe_workspace_bytes", "pe_verify_greedy", "pe_draft_readout",
+           "pe_workspace_bytes_sampled", "pe_verify_sampled",
            "pe_build_draft_batch",
            "pe_assemble_draft_inputs", "pe_step", "pe_step_early_exit", "pe_step_noalloc",
            "pe_get_tuning",
@@ -93,6 +94,11 @@ def load():
                                          P, P, P, P]
         lib.pe_draft_readout.argtypes = [P, ctypes.c_int, i64, i32, i32, P, i32, P, P, P, P]
         lib.pe_draft_readout.restype = ctypes.c_int
+        lib.pe_workspace_bytes_sampled.argtypes = [i32, i32]
+        lib.pe_workspace_bytes_sampled.restype = ctypes.c_size_t
+        lib.pe_verify_sampled.argtypes = [P, P, ctypes.c_int, i64, i64, i32, i32, i32, P, P,
+                                          ctypes.c_float, ctypes.c_uint64, P, P, P, P, P]
+        lib.pe_verify_sampled.restype = ctypes.c_int
         lib.pe_build_draft_batch.argtypes = ([i32, i32, i32, i32, i32, P, P, P, P, P, P,
                                               i32, i32] + [P] * 10)
         lib.pe_assemble_draft_inputs.argtypes = [ctypes.c_int, i32, i32, i32, i32] + [P] * 9
@@ -185,6 +191,38 @@ def verify_greedy(logits, Kp, in_tokens, accepted_len, bonus_token, workspace, e
         _dev(workspace, "workspace", torch.uint8, workspace_bytes(rows, B)),
         _dev(err, "err", torch.int32, 1), _stream(stream))
     _check(lib, rc, "pe_verify_greedy")
+
+
+def workspace_bytes_sampled(B: int, Kp: int) -> int:
+    return int(load().pe_workspace_bytes_sampled(B, Kp))
+
+
+def verify_sampled(target_logits, draft_logits, Kp, in_tokens, u_accept, temperature, seed,
+                   accepted_len, bonus_token, workspace, err, stream=None):
+    """Rejection-sampling verification of B requests: target rows B*(Kp+1),
+    draft rows B*Kp, accept coins u_accept[B*Kp], Philox seed for the draws."""
+    lib = load()
+    tp, dt, tstride = _logits(target_logits)
+    rows, V = target_logits.shape
+    if rows % (Kp + 1):
+        raise ValueError("target_logits rows must be a multiple of Kp+1")
+    B = rows // (Kp + 1)
+    if Kp:
+        dp, ddt, dstride = _logits(draft_logits)
+        if ddt != dt or draft_logits.shape[1] != V or draft_logits.shape[0] < B * Kp:
+            raise ValueError("draft_logits must be [B*Kp, V] of the target's dtype")
+    else:
+        dp, dstride = None, 0
+    rc = lib.pe_verify_sampled(
+        tp, dp, dt, tstride, dstride, B, Kp, V,
+        _dev(in_tokens, "in_tokens", torch.int32, rows if Kp else None),
+        _dev(u_accept, "u_accept", torch.float32, B * Kp if Kp else None),
+        float(temperature), int(seed) & 0xFFFFFFFFFFFFFFFF,
+        _dev(accepted_len, "accepted_len", torch.int32, B),
+        _dev(bonus_token, "bonus_token", torch.int32, B),
+        _dev(workspace, "workspace", torch.uint8, workspace_bytes_sampled(B, Kp)),
+        _dev(err, "err", torch.int32, 1), _stream(stream))
+    _check(lib, rc, "pe_verify_sampled")
 
 
 def draft_readout(logits, out_tokens, workspace, err, sample_idx=None, stream=None):

@@ -141,24 +141,22 @@ class Workload:
 
     def to(self, device) -> "Workload":
         """Copy every tensor to ``device`` (the logits keep their row stride)."""
-        def mv(t):
-            if t is None:
-                return None
-            if t.dim() == 2 and t.stride(1) == 1 and t.stride(0) != t.shape[1]:
-                base = torch.empty(t.shape[0], t.stride(0), dtype=t.dtype,
-                                   device=device)
-                base[:, : t.shape[1]].copy_(t)
-                # keep whatever sits in the padding identical too
-                pad = t.as_strided((t.shape[0], t.stride(0)), (t.stride(0), 1))
-                base.copy_(pad)
-                return base[:, : t.shape[1]]
-            return t.to(device).contiguous()
         kw = {f.name: getattr(self, f.name) for f in dataclasses.fields(self)}
         for k, v in kw.items():
             if isinstance(v, torch.Tensor):
-                kw[k] = mv(v)
+                kw[k] = _move(v, device)
         kw["extra"] = dict(self.extra)
         return Workload(**kw)
+
+
+def _move(t: torch.Tensor, device) -> torch.Tensor:
+    """Copy to ``device``; a 2-D view with padded rows keeps its row stride
+    and the padding's contents."""
+    if t.dim() == 2 and t.stride(1) == 1 and t.shape[0] and t.stride(0) != t.shape[1]:
+        base = torch.empty(t.shape[0], t.stride(0), dtype=t.dtype, device=device)
+        base.copy_(t.as_strided((t.shape[0], t.stride(0)), (t.stride(0), 1)))
+        return base[:, : t.shape[1]]
+    return t.to(device).contiguous()
 
 
 def _gen(device, seed: int) -> torch.Generator:
@@ -270,3 +268,64 @@ def make_workload(spec: WorkloadSpec | str, seed: int = 0, device="cpu") -> Work
                     block_table=bt, emb=emb, hidden=hidden, h_shared=h_shared,
                     planted_accept=planted_a, planted_bonus=planted_bonus,
                     extra={"prompt_lens": lens})
+
+
+@dataclass
+class SampledInputs:
+    """Inputs of rejection-sampling verification (request-major rows)."""
+    B: int
+    Kp: int
+    V: int
+    target_logits: torch.Tensor   # [B*(Kp+1), V]
+    draft_logits: torch.Tensor    # [B*Kp, V] (a [0, V] tensor when Kp == 0)
+    tokens: torch.Tensor          # [B*(Kp+1)] int32; row j+1 holds draft d_{j+1}
+    u_accept: torch.Tensor        # [B*Kp] float32 in [0, 1)
+
+    def to(self, device) -> "SampledInputs":
+        kw = {f.name: getattr(self, f.name) for f in dataclasses.fields(self)}
+        for k, v in kw.items():
+            if isinstance(v, torch.Tensor):
+                kw[k] = _move(v, device)
+        return SampledInputs(**kw)
+
+
+def make_sampled_inputs(B: int, Kp: int, V: int, dtype=torch.bfloat16, seed: int = 0,
+                        logits_std: float = 2.0, draft_noise: float = 0.5,
+                        plant: float = 6.0, plant_frac: float = 0.7,
+                        device="cpu") -> SampledInputs:
+    """Seeded inputs for rejection-sampling verification.
+
+    Target logits are N(0, logits_std) clamped to [-CLAMP, CLAMP]; the drafter
+    row of position j is the target row j plus N(0, draft_noise) (a drafter
+    that mostly agrees with its target).  Draft tokens are uniform over the
+    vocabulary; with probability ``plant_frac`` a draft's column is raised by
+    ``plant`` in both its target and its draft row, so that it carries most
+    of both distributions.  Each request draws from a generator of its own.
+
+    Rows are padded to a multiple of 16 bytes; the padding holds 2*PLANT, a
+    value that would dominate any distribution a read past V took part in."""
+    device = torch.device(device)
+    base_seed = int(seed) * 1_000_033 + 17
+    epv = 16 // torch.empty((), dtype=dtype).element_size()
+    stride = (V + epv - 1) // epv * epv
+    tl = torch.full((B * (Kp + 1), stride), 2 * PLANT, dtype=dtype, device=device)[:, :V]
+    dl = torch.full((B * Kp, stride), 2 * PLANT, dtype=dtype, device=device)[:, :V]
+    tokens = torch.empty(B * (Kp + 1), dtype=torch.int32, device=device)
+    u = torch.empty(B * Kp, dtype=torch.float32, device=device)
+    for b in range(B):
+        g = _gen(device, base_seed + 2 * b)
+        g_cpu = _gen("cpu", base_seed + 2 * b + 1)
+        t = _randn((Kp + 1, V), logits_std, g, device).clamp_(-CLAMP, CLAMP)
+        d = (t[:Kp] + _randn((Kp, V), draft_noise, g, device)).clamp_(-CLAMP, CLAMP)
+        toks = _randint(0, V, (Kp + 1,), g, device)
+        for j in range(Kp):
+            if torch.rand((), generator=g_cpu).item() < plant_frac:
+                x = int(toks[j + 1])
+                t[j, x] += plant
+                d[j, x] += plant
+        tl[b * (Kp + 1):(b + 1) * (Kp + 1)] = t.to(dtype)
+        dl[b * Kp:(b + 1) * Kp] = d.to(dtype)
+        tokens[b * (Kp + 1):(b + 1) * (Kp + 1)] = toks.to(torch.int32)
+        u[b * Kp:(b + 1) * Kp] = torch.rand((Kp,), generator=g, device=device)
+    return SampledInputs(B=B, Kp=Kp, V=V, target_logits=tl, draft_logits=dl,
+                         tokens=tokens, u_accept=u)
