@@ -411,6 +411,130 @@ def run_ours(args):
     return 0
 
 
+SAMPLED_METRIC = "rejection-sampling verification logits rows/s"
+SAMPLED_SHAPE = {"B": 256, "Kp": 7, "V": 151936}  # the large-batch decode shape
+
+
+def sampled_bytes(B, Kp, V, elt, rejected: int) -> dict:
+    """Bytes the two-pass rejection-sampling verification must move: every
+    target and draft row once (statistics, probabilities, bonus-row draw),
+    then the target and draft row at the rejected position of each request
+    with a rejection again (the residual needs both rows' normalisers before
+    it can be drawn), plus tokens, coins and the two outputs."""
+    rows = B * (Kp + 1) + B * Kp
+    parts = {"logits": rows * V * elt, "residual_reread": rejected * 2 * V * elt,
+             "metadata": 4 * B * (Kp + 1) + 4 * B * Kp + 8 * B}
+    parts["total"] = sum(parts.values())
+    return parts
+
+
+def run_sampled(args):
+    """Time pe_verify_sampled (two launches per step) on the large-batch
+    decode shape: B=256, K'=7, V=151936, bf16, temperature --temperature."""
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    from speculative_decoding_pe_gb300 import _native
+    _native.load()
+    B, Kp, V = SAMPLED_SHAPE["B"], SAMPLED_SHAPE["Kp"], SAMPLED_SHAPE["V"]
+    seed = 7100 + rank
+    s = wl.make_sampled_inputs(B, Kp, V, dtype=torch.bfloat16, seed=seed, device=device)
+    acc = torch.empty(B, dtype=torch.int32, device=device)
+    bon = torch.empty(B, dtype=torch.int32, device=device)
+    ws = torch.zeros(_native.workspace_bytes_sampled(B, Kp), dtype=torch.uint8, device=device)
+    err = _native.new_error_word(device)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    T = args.temperature
+
+    def step():
+        _native.verify_sampled(s.target_logits, s.draft_logits, Kp, s.tokens, s.u_accept, T,
+                               1234 + rank, acc, bon, ws, err, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(device)
+    if int(err.item()) != 0 or int(ws.count_nonzero()) != 0:
+        raise SystemExit("device error word or workspace not zero after warm-up")
+    sampler = ClockSampler(local)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(device)
+    t_wall0 = time.time()
+    torch.cuda.nvtx.range_push("timed")
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize(device)
+    barrier(world)
+    t_wall1 = time.time()
+    clocks = sampler.stop(t_wall0, t_wall1)
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    mean_ms = sum(step_ms) / len(step_ms)
+    rows = B * (Kp + 1) + B * Kp
+    value, mean_ms_max, _ = aggregate(float(rows), mean_ms, world, device)
+    rejected = int((acc < Kp).sum())
+    bytes_ = sampled_bytes(B, Kp, V, 2, rejected)
+    peak, peak_kind = measured_peak()
+    achieved = bytes_["total"] / (mean_ms / 1e3) / 1e9
+
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_baseline:
+        import oracle  # CPU baseline leg only
+        host = s.to("cpu")
+        nreq = 4
+        sub = wl.SampledInputs(B=nreq, Kp=Kp, V=V,
+                               target_logits=host.target_logits[:nreq * (Kp + 1)],
+                               draft_logits=host.draft_logits[:nreq * Kp],
+                               tokens=host.tokens[:nreq * (Kp + 1)],
+                               u_accept=host.u_accept[:nreq * Kp])
+        times = []
+        t_end = time.time() + args.cpu_budget
+        while len(times) < 3 or time.time() < t_end:
+            t0 = time.perf_counter()
+            oracle.verify_sampled(sub.target_logits, sub.draft_logits, nreq, Kp, sub.tokens,
+                                  sub.u_accept, T, 1234)
+            times.append(time.perf_counter() - t0)
+        t = statistics.median(times)
+        cpu = {"value": nreq * (2 * Kp + 1) / t, "unit": "rows/s", "cores": 1,
+               "kind": "oracle",
+               "sample": "first %d of %d requests, %d runs, median %.1f ms, "
+                         "single-threaded C oracle on %s" % (
+                             nreq, B, len(times), t * 1e3, cpu_model())}
+    if rank == 0:
+        print(json.dumps({
+            "metric": SAMPLED_METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "rejection-sampling verification B=%d K'=%d V=%d bf16 "
+                                   "T=%g" % (B, Kp, V, T),
+                       "accepted_len_histogram": torch.bincount(
+                           acc.long().cpu(), minlength=Kp + 1).tolist(),
+                       "l2": "flushed between steps (2x L2 written)",
+                       "median_us": statistics.median(step_ms) * 1e3,
+                       "min_us": min(step_ms) * 1e3},
+            "us_per_step": mean_ms_max * 1e3,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
+                         "algorithmic_bytes_per_launch": bytes_["total"],
+                         "bytes": bytes_,
+                         "kernel": "pe::sampled_stats_kernel + pe::sampled_residual_kernel "
+                                   "(one call, two launches)"},
+            "cpu_baseline": cpu, "gpu_launches": 2 * args.steps, "clocks": clocks}))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def measure_e2e(w, out, ws, err, packed, stream, device, args):
     """The same step through the public API with inputs copied in from pinned
     host memory and the per-request results copied back, every step."""
@@ -515,6 +639,10 @@ def main(argv=None):
     ap.add_argument("--early-exit", action="store_true",
                     help="time pe_step_early_exit (rows after each request's first "
                          "mismatch are not read)")
+    ap.add_argument("--sampled", action="store_true",
+                    help="time rejection-sampling verification (pe_verify_sampled) "
+                         "instead of the fused greedy step")
+    ap.add_argument("--temperature", type=float, default=1.0)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
@@ -524,6 +652,8 @@ def main(argv=None):
         raise SystemExit("--warmup must be at least 3")
     if args.impl == "reference":
         return run_reference(args)
+    if args.sampled:
+        return run_sampled(args)
     return run_ours(args)
 
 

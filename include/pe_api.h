@@ -142,7 +142,7 @@ size_t pe_workspace_bytes_sampled(int32_t B, int32_t Kp);
  *   row b(Kp+1)+Kp) when a_b = Kp.
  * Draws are Gumbel-max: the column maximising s(v) + G_b(v), s(v) = log of
  * the (unnormalised) weight of column v, G_b(v) = -log(-log(U)),
- * U = ((w >> 8) + 0.5) / 2^24 and w = word (v mod 4) of Philox4x32-10
+ * U = ((w >> 9) + 0.5) / 2^23 (exact in fp32) and w = word (v mod 4) of Philox4x32-10
  * (Salmon et al., SC'11) at counter (v/4, b, 0, 0) under the key (low,
  * high word of `seed`).  Only the accept/reject coins come from the caller.
  *  target_logits [B*(Kp+1), V], row stride target_stride elements.

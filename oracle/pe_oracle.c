@@ -182,7 +182,9 @@ static double gumbel(uint64_t seed, uint32_t stream, int32_t i) {
   key[0] = (uint32_t)seed;
   key[1] = (uint32_t)(seed >> 32);
   oracle_philox4x32_10(ctr, key, w);
-  u = ((double)(w[i & 3] >> 8) + 0.5) / 16777216.0; /* 24 bits: exact in fp32 */
+  /* 23 bits: (k + 0.5) / 2^23 needs 24 significant bits, so U is exact in
+   * fp32 as well and lies in [2^-24, 1 - 2^-24] */
+  u = ((double)(w[i & 3] >> 9) + 0.5) / 8388608.0;
   return -log(-log(u));
 }
 

@@ -62,7 +62,7 @@ void oracle_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2],
  * the bonus is drawn from max(0, p - q) (from p when that is all zero);
  * when every draft is accepted a_b = Kp and the bonus is drawn from
  * softmax(target row b(Kp+1)+Kp / temperature).  Draws use the Gumbel-max
- * rule with noise -log(-log(U)), U = ((w >> 8) + 0.5) / 2^24, w = word (i mod 4)
+ * rule with noise -log(-log(U)), U = ((w >> 9) + 0.5) / 2^23, w = word (i mod 4)
  * of Philox4x32-10(counter = (i / 4, b, 0, 0), key = (seed lo, seed hi)).
  * A draft token outside [0, V) is rejected. */
 int oracle_verify_sampled(const void* target_logits, const void* draft_logits,

@@ -62,7 +62,7 @@ def run_oracle(s, T, seed):
 
 def _gumbel(seed, b, v):
     w = oracle.philox4x32_10((v // 4, b, 0, 0), (seed & 0xFFFFFFFF, seed >> 32))[v % 4]
-    u = ((w >> 8) + 0.5) / 16777216.0
+    u = ((w >> 9) + 0.5) / 8388608.0
     return -math.log(-math.log(u))
 
 
