@@ -1,6 +1,8 @@
 // Internal helpers of libpe.so (device and host).  Not part of the ABI.
 #pragma once
 
+#include <atomic>
+
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -105,6 +107,21 @@ inline bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 inline int elt_size(int dtype) { return dtype == PE_F32 ? 4 : dtype == PE_BF16 ? 2 : 0; }
 inline int launch_status() {
   return cudaGetLastError() == cudaSuccess ? PE_OK : PE_ECUDA;
+}
+
+// Dynamic shared memory above 48 KiB must be opted into once per kernel and
+// device (a host-side attribute; no synchronisation).
+template <class K>
+bool allow_smem(K kernel, int bytes, std::atomic<unsigned long long>& done_mask) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
+  const unsigned long long bit = 1ull << dev;
+  if (done_mask.load(std::memory_order_relaxed) & bit) return true;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+      cudaSuccess)
+    return false;
+  done_mask.fetch_or(bit);
+  return true;
 }
 
 }  // namespace pe_host

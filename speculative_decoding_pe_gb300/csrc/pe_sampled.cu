@@ -23,13 +23,15 @@
 //     max(0, p - q) (and, should that be empty, from p).
 // Everything is compared in the log2 domain: argmax of y(v) + G(v) log2(e)
 // is argmax of logit(v) / T + G(v), and G(v) log2(e) = -log2(E(v)) with
-// E = -ln U.  Draws use U from Philox4x32-10 (Salmon et al., SC'11),
+// E = -ln U (computed as -log2 U, a constant multiple).  Draws use U from Philox4x32-10 (Salmon et al., SC'11),
 // counter (v / 4, request, 0, 0), key = the seed's two words.
 #include "pe_internal.cuh"
 
 namespace pe {
 
-constexpr int kMaxChunksSampled = 16;  // chunks per row (partial stats slots)
+constexpr int kMaxChunksSampled = 32;  // warp units per row (partial stats slots)
+constexpr int kStatsChunkVecs = 1024;  // vectors per stats unit (16 KB), at least
+constexpr int kResidChunkVecs = 256;   // vectors per residual unit and row (4 KB)
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct SampledParams {
@@ -82,6 +84,25 @@ __device__ __forceinline__ uint32_t word(uint4 w, int k) {
   return (k & 2) ? hi : lo;
 }
 
+// Packed fp32 pairs (Blackwell's two-wide FP32 SIMD): (d0, d1) = (a * b + c)
+// and (a + b) lane by lane, one instruction for both.
+__device__ __forceinline__ void fma2(float& d0, float& d1, float a0, float a1, float b0,
+                                     float b1, float c0, float c1) {
+  asm("{\n\t.reg .b64 pa, pb, pc, pd;\n\t"
+      "mov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\tmov.b64 pc, {%6, %7};\n\t"
+      "fma.rn.f32x2 pd, pa, pb, pc;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+__device__ __forceinline__ void add2(float& d0, float& d1, float a0, float a1, float b0,
+                                     float b1) {
+  asm("{\n\t.reg .b64 pa, pb, pd;\n\t"
+      "mov.b64 pa, {%2, %3};\n\tmov.b64 pb, {%4, %5};\n\t"
+      "add.rn.f32x2 pd, pa, pb;\n\tmov.b64 {%0, %1}, pd;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ float ex2(float x) {  // 2^x, subnormal results flushed
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -93,15 +114,45 @@ __device__ __forceinline__ float lg2(float x) {  // log2 x (approximate)
   return y;
 }
 
-// Gumbel noise of one Philox word in the log2 domain: G log2(e) = -log2(E),
-// E = -ln U, U = ((w >> 9) + 0.5) / 2^23.  U is formed exactly: the 23 bits
-// become the mantissa of a float in [1, 2) and one subtraction (exact, the
-// result needs 24 significant bits) shifts it to [2^-24, 1 - 2^-24].  The
-// inner logarithm is CUDA's logf, accurate near U = 1 where E is tiny.
+// Gumbel noise of one Philox word in the log2 domain, up to a constant that
+// shifts every score of a draw alike: -log2(E2) with E2 = -log2 U = E log2(e),
+// E = -ln U, U = ((w >> 9) + 0.5) / 2^23.  U and t = 1 - U are formed exactly:
+// 23 bits (k, and 2^23 - 1 - k) become the mantissa of a float in [1, 2) and
+// one exact subtraction shifts it to [2^-24, 1 - 2^-24].  E2 needs a small
+// RELATIVE error: below t = 1/64 it is the series log2(e) (t + t^2/2 + ... +
+// t^5/5) of -log2(1 - t) (truncation error under t^4/6 relative); above, the
+// hardware log2 has absolute error near 2^-22, relative error under 1e-5 of
+// an E2 that is then at least 0.0227.
 __device__ __forceinline__ float noise2(uint32_t w) {
-  const float f = __uint_as_float((w >> 9) | 0x3f800000u);
-  const float u = f - (1.0f - 5.9604644775390625e-8f);  // (k + 0.5) / 2^23
-  return -lg2(-logf(u));
+  constexpr float kOneMinus = 1.0f - 5.9604644775390625e-8f;  // 1 - 2^-24
+  const uint32_t k = w >> 9;
+  const float u = __uint_as_float(k | 0x3f800000u) - kOneMinus;
+  const float t = __uint_as_float((k ^ 0x7fffffu) | 0x3f800000u) - kOneMinus;
+  const float series =
+      t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, kLog2e / 5.f, kLog2e / 4.f), kLog2e / 3.f),
+                       kLog2e / 2.f),
+               kLog2e);
+  const float e2 = t < 0.015625f ? series : -lg2(u);
+  return -lg2(e2);
+}
+
+// t = 1 - U of one Philox word, exact (see noise2).
+__device__ __forceinline__ float one_minus_u(uint32_t w) {
+  return __uint_as_float(((w >> 9) ^ 0x7fffffu) | 0x3f800000u) - (1.0f - 5.9604644775390625e-8f);
+}
+
+// Pruning bound.  -ln(1 - t) >= t, so E2 = -log2 U >= t log2(e) and a
+// column's score y - log2(E2) is at most y - log2(t log2(e)).  With
+// e = 2^(y - m) a column can only exceed a threshold thr when
+// e > 2^(thr - m) log2(e) t; columns failing that test are skipped without
+// computing their noise.  kBound keeps the test conservative by far more
+// than the rounding of the quantities it compares.
+constexpr float kBound = 1.4426950408889634f * (1.0f - 1.0f / 4096.0f);
+
+__device__ __forceinline__ float warp_max_f(float x) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+  return x;
 }
 
 // ----------------------------------------------------------- element access
@@ -191,104 +242,98 @@ struct Best {
   }
 };
 
-struct SampledShared {
-  float2 red[kWarps];
-  unsigned long long kred[kWarps];
-  int unit;
-  int acc;
-  int fallback;
-};
-
 // Virtual row vr: target rows [0, Rt), then draft rows [Rt, Rt + Rd).
 __device__ __forceinline__ const char* vrow_ptr(const SampledParams& p, int vr) {
   return vr < p.Rt ? static_cast<const char*>(p.tlogits) + (long long)vr * p.t_row_bytes
                    : static_cast<const char*>(p.dlogits) + (long long)(vr - p.Rt) * p.d_row_bytes;
 }
 
-// Block-wide maximum key; valid in thread 0.
-__device__ __forceinline__ unsigned long long block_max_key(SampledShared& sh,
-                                                            unsigned long long k) {
-  const int tid = threadIdx.x;
-  k = warp_max_key(k);
-  if ((tid & 31) == 0) sh.kred[tid >> 5] = k;
-  __syncthreads();
-  if (tid < 32) {
-    k = tid < kWarps ? sh.kred[tid] : 0ull;
-    k = warp_max_key(k);
-  }
-  __syncthreads();
-  return k;
-}
-
 }  // namespace pe
 
 namespace pe {
 
+// Every unit of work below belongs to ONE warp: a warp takes a unit from the
+// dynamic counter, streams it, reduces with shuffles and publishes its
+// result with atomics.  No CTA barrier anywhere, so each warp keeps its
+// loads in flight regardless of what the other warps of its CTA are doing.
+
 // One row chunk folded into (m, s) = (max, sum of 2^(y - max)) with
-// y = logit * c2, and, for the bonus row (draw), into the thread's best
-// Gumbel score y + G log2(e).  Vectors past the chunk read as -inf.
-template <int DT>
+// y = logit * c2, and, for the bonus row (DRAW), into the lane's best Gumbel
+// score y + G log2(e), pruned by the bound above against the best score of
+// the warp (shared after every batch).  Vectors past the chunk read as -inf
+// and contribute nothing.  The bonus row takes half the vectors per batch:
+// the noise needs the registers.
+template <int DT, bool DRAW>
 __device__ __forceinline__ void fold_chunk(const SampledParams& p, const char* rowp, int v_lo,
-                                           int v_hi, bool tail, bool draw, int b, float& m,
-                                           float& s, Best& best) {
+                                           int v_hi, int b, int lane, float& m, float& s,
+                                           Best& best) {
   using E = Vec<DT>;
-  const int tid = threadIdx.x;
+  constexpr int kV = DRAW ? kVecPerThread / 2 : kVecPerThread;
   const uint4* row = reinterpret_cast<const uint4*>(rowp);
   const uint4 neg = make_uint4(E::kNegInf, E::kNegInf, E::kNegInf, E::kNegInf);
-  for (int base = v_lo; base < v_hi; base += kBatchVecs) {
-    if (base + tid >= v_hi) break;
-    uint4 x[kVecPerThread];
+  float thr = -INFINITY;
+  for (int base = v_lo; base < v_hi; base += 32 * kV) {
+    uint4 x[kV];
+    if (base + 32 * kV <= v_hi) {  // a whole batch: no bounds to check
 #pragma unroll
-    for (int i = 0; i < kVecPerThread; ++i) {
-      const int v = base + i * kThreads + tid;
-      x[i] = v < v_hi ? __ldcs(row + v) : neg;
+      for (int i = 0; i < kV; ++i) x[i] = __ldcs(row + base + i * 32 + lane);
+    } else {
+#pragma unroll
+      for (int i = 0; i < kV; ++i) {
+        const int v = base + i * 32 + lane;
+        x[i] = v < v_hi ? __ldcs(row + v) : neg;
+      }
     }
     uint32_t mr = E::max_init();
 #pragma unroll
-    for (int i = 0; i < kVecPerThread; ++i) mr = E::max_fold(mr, x[i]);
+    for (int i = 0; i < kV; ++i) mr = E::max_fold(mr, x[i]);
     const float bm = E::max_value(mr) * p.c2;  // monotone: max of the scaled values
     if (bm > m) {
       s *= ex2(m - bm);
       m = bm;
     }
+    if (!DRAW) {  // pairs of elements: two sums, packed arithmetic
+      float s1 = 0.f;
 #pragma unroll
-    for (int i = 0; i < kVecPerThread; ++i) {
-      float z[E::kN];
-      E::unpack(x[i], z);
+      for (int i = 0; i < kV; ++i) {
+        float z[E::kN];
+        E::unpack(x[i], z);
 #pragma unroll
-      for (int e = 0; e < E::kN; ++e) s += ex2(fmaf(z[e], p.c2, -m));
-    }
-    if (draw) {
+        for (int e = 0; e < E::kN; e += 2) {
+          float y0, y1;
+          fma2(y0, y1, z[e], z[e + 1], p.c2, p.c2, -m, -m);
+          add2(s, s1, s, s1, ex2(y0), ex2(y1));
+        }
+      }
+      s += s1;
+    } else {
+      float K = ex2(thr - m) * kBound;
 #pragma unroll
-      for (int i = 0; i < kVecPerThread; ++i) {
-        const int v = base + i * kThreads + tid;
-        if (v >= v_hi) continue;
+      for (int i = 0; i < kV; ++i) {
+        const int v = base + i * 32 + lane;
         float z[E::kN];
         E::unpack(x[i], z);
 #pragma unroll
         for (int g = 0; g < E::kN / 4; ++g) {
           const uint4 w = philox(p, (uint32_t)((v * E::kN) / 4 + g), (uint32_t)b);
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            best.offer(z[4 * g + k] * p.c2 + noise2(ws[k]), v * E::kN + 4 * g + k);
+          for (int k = 0; k < 4; ++k) {
+            const float y = z[4 * g + k] * p.c2;
+            const float ev = ex2(y - m);
+            s += ev;
+            const uint32_t wk = word(w, k);
+            if (ev > K * one_minus_u(wk)) {  // may beat the threshold
+              const float sc = y + noise2(wk);
+              best.offer(sc, v * E::kN + 4 * g + k);
+              if (sc > thr) {
+                thr = sc;
+                K = ex2(thr - m) * kBound;
+              }
+            }
+          }
         }
       }
-    }
-  }
-  if (tail && tid == 0) {  // elements after the last whole vector
-    for (int e = 0; e < p.tail; ++e) {
-      const int col = p.nvec * E::kN + e;
-      const float y = E::at(rowp, col) * p.c2;
-      if (y > m) {
-        s *= ex2(m - y);
-        m = y;
-      }
-      s += ex2(y - m);
-      if (draw) {
-        const uint4 w = philox(p, (uint32_t)(col / 4), (uint32_t)b);
-        best.offer(y + noise2(word(w, col & 3)), col);
-      }
+      thr = warp_max_f(thr);
     }
   }
 }
@@ -322,107 +367,132 @@ __device__ __forceinline__ void decide(const SampledParams& p, int b) {
   }
 }
 
+// The end of a unit (row vr, chunk c): the scalar tail of the row, the
+// warp's reduction and its publication.  The warp that completes a row
+// merges its partials (lane-strided, then a shuffle tree: a fixed order, so
+// the result does not depend on timing), stores the row's log2-normaliser
+// and the draft token's probability; the warp that completes a request
+// decides its accepted length.
 template <int DT>
-__device__ __forceinline__ void stats_unit(const SampledParams& p, SampledShared& sh, int u) {
+__device__ __forceinline__ void stats_finish(const SampledParams& p, int vr, int c, int lane,
+                                             float m, float s, const Best& best) {
   using E = Vec<DT>;
-  const int tid = threadIdx.x;
-  const int vr = u / p.C;
-  const int c = u - vr * p.C;
   int b, j;
   if (vr < p.Rt) {
     b = vr / (p.Kp + 1);
     j = vr - b * (p.Kp + 1);
   } else {
     b = (vr - p.Rt) / p.Kp;
-    j = -1;  // draft row
+    j = (vr - p.Rt) - b * p.Kp;
   }
-  const bool draw = j == p.Kp;  // the bonus row
+  const bool draw = vr < p.Rt && j == p.Kp;  // the bonus row
   const char* rowp = vrow_ptr(p, vr);
-  const int v_lo = c * p.chunk_vecs;
-  const int v_hi = min(v_lo + p.chunk_vecs, p.nvec);
-  float m = -INFINITY, s = 0.f;
-  Best best;
-  fold_chunk<DT>(p, rowp, v_lo, v_hi, p.tail && c == p.C - 1, draw, b, m, s, best);
-
-  const float2 st = warp_combine(make_float2(m, s));
-  if ((tid & 31) == 0) sh.red[tid >> 5] = st;
-  unsigned long long gk = 0ull;
-  if (draw) gk = block_max_key(sh, best.key());  // includes the barrier
-  else __syncthreads();
-  if (tid < 32) {
-    float2 t = tid < kWarps ? sh.red[tid] : make_float2(-INFINITY, 0.f);
-    t = warp_combine(t);
-    if (tid == 0) {
-      p.partial[vr * kMaxChunksSampled + c] = t;
-      if (draw) atomicMax(p.gkey + b, gk);
-      __threadfence();
-      if (atomicAdd(p.rcount + vr, 1u) == (unsigned)(p.C - 1)) {  // row complete
-        atomicExch(p.rcount + vr, 0u);
-        float2 acc = __ldcg(p.partial + vr * kMaxChunksSampled);
-        for (int cc = 1; cc < p.C; ++cc)  // chunk order: deterministic
-          acc = combine(acc, __ldcg(p.partial + vr * kMaxChunksSampled + cc));
-        for (int cc = 0; cc < p.C; ++cc)
-          p.partial[vr * kMaxChunksSampled + cc] = make_float2(0.f, 0.f);
-        const float L = acc.x + log2f(acc.y);  // log2 of sum of 2^y
-        p.lse[vr] = L;
-        if (!draw) {  // probability of the row's draft token
-          const int jj = vr < p.Rt ? j : (vr - p.Rt) - b * p.Kp;
-          const int x = __ldg(p.tokens + b * (p.Kp + 1) + jj + 1);
-          p.prob[vr] = (x >= 0 && x < p.V) ? ex2(E::at(rowp, x) * p.c2 - L) : -1.f;
-        }
-        __threadfence();
-        if (atomicAdd(p.qcount + b, 1u) == (unsigned)(2 * p.Kp)) {  // all 2Kp+1 rows
-          atomicExch(p.qcount + b, 0u);
-          __threadfence();
-          decide(p, b);
-        }
+  Best bt = best;
+  if (p.tail && c == p.C - 1 && lane == 0) {  // elements after the last whole vector
+    for (int e = 0; e < p.tail; ++e) {
+      const int col = p.nvec * E::kN + e;
+      const float y = E::at(rowp, col) * p.c2;
+      if (y > m) {
+        s *= ex2(m - y);
+        m = y;
+      }
+      s += ex2(y - m);
+      if (draw) {
+        const uint4 w = philox(p, (uint32_t)(col / 4), (uint32_t)b);
+        bt.offer(y + noise2(word(w, col & 3)), col);
       }
     }
   }
-  __syncthreads();
+  const float2 t = warp_combine(make_float2(m, s));
+  const unsigned long long gk = draw ? warp_max_key(bt.key()) : 0ull;
+  int last = 0;
+  if (lane == 0) {
+    p.partial[vr * kMaxChunksSampled + c] = t;
+    if (draw) atomicMax(p.gkey + b, gk);
+    __threadfence();
+    last = atomicAdd(p.rcount + vr, 1u) == (unsigned)(p.C - 1);
+  }
+  if (!__shfl_sync(0xffffffffu, last, 0)) return;
+  __threadfence();
+  float2 acc = make_float2(-3.0e38f, 0.f);
+  for (int cc = lane; cc < p.C; cc += 32) {
+    acc = combine(acc, __ldcg(p.partial + vr * kMaxChunksSampled + cc));
+    p.partial[vr * kMaxChunksSampled + cc] = make_float2(0.f, 0.f);
+  }
+  acc = warp_combine(acc);
+  if (lane == 0) {
+    p.rcount[vr] = 0u;
+    const float L = acc.x + log2f(acc.y);  // log2 of the sum of 2^y
+    p.lse[vr] = L;
+    if (!draw) {  // probability of the row's draft token
+      const int x = __ldg(p.tokens + b * (p.Kp + 1) + j + 1);
+      p.prob[vr] = (x >= 0 && x < p.V) ? ex2(E::at(rowp, x) * p.c2 - L) : -1.f;
+    }
+    __threadfence();
+    if (atomicAdd(p.qcount + b, 1u) == (unsigned)(2 * p.Kp)) {  // all 2Kp+1 rows
+      p.qcount[b] = 0u;
+      __threadfence();
+      decide(p, b);
+    }
+  }
 }
 
+// Stats of one warp unit u = row * C + chunk.
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 3) sampled_stats_kernel(const SampledParams p) {
-  __shared__ SampledShared sh;
+__device__ __forceinline__ void stats_unit(const SampledParams& p, int u, int lane) {
+  const int vr = u / p.C;
+  const int c = u - vr * p.C;
+  const int b = vr < p.Rt ? vr / (p.Kp + 1) : (vr - p.Rt) / p.Kp;
+  const bool draw = vr < p.Rt && vr - b * (p.Kp + 1) == p.Kp;  // the bonus row
+  const char* rowp = vrow_ptr(p, vr);
+  const int v_lo = c * p.chunk_vecs;
+  const int v_hi = min(v_lo + p.chunk_vecs, p.nvec);
+  float m = -3.0e38f, s = 0.f;  // finite: an empty lane never forms -inf + inf
+  Best best;
+  if (draw) fold_chunk<DT, true>(p, rowp, v_lo, v_hi, b, lane, m, s, best);
+  else fold_chunk<DT, false>(p, rowp, v_lo, v_hi, b, lane, m, s, best);
+  stats_finish<DT>(p, vr, c, lane, m, s, best);
+}
+
+// Persistent warps over a dynamic unit counter (sched[0]); the next unit is
+// fetched before the current one is processed.  The last warp to leave
+// resets the counter words (sched[0], sched[1]).
+constexpr int kStatsCtasPerSm = 4;  // 32 warps per SM: 64 registers a thread
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, kStatsCtasPerSm) sampled_stats_kernel(
+    const SampledParams p) {
+  const int lane = threadIdx.x & 31;
   const int n_units = (p.Rt + p.Rd) * p.C;
-  int u = blockIdx.x;
+  int u = 0;
+  if (lane == 0) u = (int)atomicAdd(p.sched, 1u);
+  u = __shfl_sync(0xffffffffu, u, 0);
   while (u < n_units) {
-    unsigned next = 0;
-    if (threadIdx.x == 0) next = gridDim.x + atomicAdd(p.sched, 1u);
-    stats_unit<DT>(p, sh, u);
-    if (threadIdx.x == 0) sh.unit = (int)next;
-    __syncthreads();
-    u = sh.unit;
-    __syncthreads();
+    int next = 0;
+    if (lane == 0) next = (int)atomicAdd(p.sched, 1u);
+    stats_unit<DT>(p, u, lane);
+    u = __shfl_sync(0xffffffffu, next, 0);
   }
-  if (threadIdx.x == 0) {
+  if (lane == 0) {
     __threadfence();
-    if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {
+    if (atomicAdd(p.sched + 1, 1u) == gridDim.x * kWarps - 1) {
       atomicExch(p.sched, 0u);
       atomicExch(p.sched + 1, 0u);
     }
   }
 }
 
-}  // namespace pe
-
-namespace pe {
-
-// Residual draw of request b, chunk c: Gumbel-max over log2 max(0, p - q)
-// with p = 2^(y_t - L_t), q = 2^(y_d - L_d).  The unit that completes the
-// request publishes the draw; should the residual be empty (p == q
-// everywhere, possible only for identical rows) that CTA draws from p over
-// the whole target row instead.
+// Residual draw of request b, chunk c (warp unit u = b * C2 + c): Gumbel-max
+// over log2 max(0, p - q) with p = 2^(y_t - L_t), q = 2^(y_d - L_d).  The
+// warp that completes the request publishes the draw; should the residual be
+// empty (p == q everywhere, possible only for identical rows) that warp
+// draws from p over the whole target row instead.
 template <int DT>
-__device__ __forceinline__ void residual_unit(const SampledParams& p, SampledShared& sh, int u) {
+__device__ __forceinline__ void residual_unit(const SampledParams& p, int u, int lane) {
   using E = Vec<DT>;
-  const int tid = threadIdx.x;
   const int b = u / p.C2;
   const int c = u - b * p.C2;
-  if (tid == 0) sh.acc = __ldcg(p.acc + b);
-  __syncthreads();
-  const int a = sh.acc;
+  const int a = __ldcg(p.acc + b);
   const bool draw = a < p.Kp;  // else the stats pass drew the bonus already
   const int vt = b * (p.Kp + 1) + a;
   const int vd = p.Rt + b * p.Kp + a;
@@ -437,18 +507,19 @@ __device__ __forceinline__ void residual_unit(const SampledParams& p, SampledSha
     const int v_lo = c * p.chunk2_vecs;
     const int v_hi = min(v_lo + p.chunk2_vecs, p.nvec);
     constexpr int kV = kVecPerThread / 2;  // two rows: half the vectors each
-    for (int base = v_lo; base < v_hi; base += kThreads * kV) {
-      if (base + tid >= v_hi) break;
+    float thr = -INFINITY;  // best score of the warp so far (absolute log2 units)
+    for (int base = v_lo; base < v_hi; base += 32 * kV) {
+      const float K = ex2(thr) * kBound;  // d > K t: the column may beat thr
       uint4 xt[kV], xd[kV];
 #pragma unroll
       for (int i = 0; i < kV; ++i) {
-        const int v = base + i * kThreads + tid;
+        const int v = base + i * 32 + lane;
         xt[i] = v < v_hi ? __ldcs(tr + v) : make_uint4(0u, 0u, 0u, 0u);
         xd[i] = v < v_hi ? __ldcs(dr + v) : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
       for (int i = 0; i < kV; ++i) {
-        const int v = base + i * kThreads + tid;
+        const int v = base + i * 32 + lane;
         if (v >= v_hi) continue;
         float zt[E::kN], zd[E::kN];
         E::unpack(xt[i], zt);
@@ -456,17 +527,22 @@ __device__ __forceinline__ void residual_unit(const SampledParams& p, SampledSha
 #pragma unroll
         for (int g = 0; g < E::kN / 4; ++g) {
           const uint4 w = philox(p, (uint32_t)((v * E::kN) / 4 + g), (uint32_t)b);
-          const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int e = 4 * g + k;
             const float d = ex2(fmaf(zt[e], p.c2, -Lt)) - ex2(fmaf(zd[e], p.c2, -Ld));
-            if (d > 0.f) best.offer(lg2(d) + noise2(ws[k]), v * E::kN + e);
+            const uint32_t wk = word(w, k);
+            if (d > K * one_minus_u(wk)) {  // d > 0 and the column may beat thr
+              const float sc = lg2(d) + noise2(wk);
+              best.offer(sc, v * E::kN + e);
+              thr = fmaxf(thr, sc);
+            }
           }
         }
       }
+      thr = warp_max_f(thr);
     }
-    if (p.tail && c == p.C2 - 1 && tid == 0) {
+    if (p.tail && c == p.C2 - 1 && lane == 0) {
       for (int e = 0; e < p.tail; ++e) {
         const int col = p.nvec * E::kN + e;
         const float d = ex2(fmaf(E::at(trow, col), p.c2, -Lt)) -
@@ -478,54 +554,55 @@ __device__ __forceinline__ void residual_unit(const SampledParams& p, SampledSha
       }
     }
   }
-  const unsigned long long k = block_max_key(sh, best.key());
-  if (tid == 0) {
-    sh.fallback = 0;
+  const unsigned long long k = warp_max_key(best.key());
+  int last = 0;
+  if (lane == 0) {
     if (draw) atomicMax(p.rkey + b, k);
     __threadfence();
-    if (atomicAdd(p.dcount + b, 1u) == (unsigned)(p.C2 - 1)) {  // every unit of b is done
-      atomicExch(p.dcount + b, 0u);
-      p.acc[b] = 0;
-      if (draw) {
-        const unsigned long long r = atomicExch(p.rkey + b, 0ull);
-        if (r) p.bonus_token[b] = (int)key_col(r);
-        else sh.fallback = 1;
-        p.lse[vt] = 0.f;
-        p.lse[vd] = 0.f;
-      }
+    last = atomicAdd(p.dcount + b, 1u) == (unsigned)(p.C2 - 1);  // every unit of b is done
+  }
+  if (!__shfl_sync(0xffffffffu, last, 0)) return;
+  __threadfence();
+  int fallback = 0;
+  if (lane == 0) {
+    p.dcount[b] = 0u;
+    p.acc[b] = 0;
+    if (draw) {
+      const unsigned long long r = atomicExch(p.rkey + b, 0ull);
+      if (r) p.bonus_token[b] = (int)key_col(r);
+      else fallback = 1;
+      p.lse[vt] = 0.f;
+      p.lse[vd] = 0.f;
     }
   }
-  __syncthreads();
-  if (sh.fallback) {  // empty residual: draw from p (rare; one CTA, whole row)
+  if (__shfl_sync(0xffffffffu, fallback, 0)) {  // empty residual: draw from p (rare)
     const char* trow = vrow_ptr(p, vt);
     Best bp;
-    for (int col = tid; col < p.V; col += kThreads) {
+    for (int col = lane; col < p.V; col += 32) {
       const uint4 w = philox(p, (uint32_t)(col / 4), (uint32_t)b);
       bp.offer(E::at(trow, col) * p.c2 + noise2(word(w, col & 3)), col);
     }
-    const unsigned long long kf = block_max_key(sh, bp.key());
-    if (tid == 0) p.bonus_token[b] = (int)key_col(kf);
+    const unsigned long long kf = warp_max_key(bp.key());
+    if (lane == 0) p.bonus_token[b] = (int)key_col(kf);
   }
-  __syncthreads();
 }
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 3) sampled_residual_kernel(const SampledParams p) {
-  __shared__ SampledShared sh;
+  const int lane = threadIdx.x & 31;
   const int n_units = p.B * p.C2;
-  int u = blockIdx.x;
+  int u = 0;
+  if (lane == 0) u = (int)atomicAdd(p.sched + 2, 1u);
+  u = __shfl_sync(0xffffffffu, u, 0);
   while (u < n_units) {
-    unsigned next = 0;
-    if (threadIdx.x == 0) next = gridDim.x + atomicAdd(p.sched + 2, 1u);
-    residual_unit<DT>(p, sh, u);
-    if (threadIdx.x == 0) sh.unit = (int)next;
-    __syncthreads();
-    u = sh.unit;
-    __syncthreads();
+    int next = 0;
+    if (lane == 0) next = (int)atomicAdd(p.sched + 2, 1u);
+    residual_unit<DT>(p, u, lane);
+    u = __shfl_sync(0xffffffffu, next, 0);
   }
-  if (threadIdx.x == 0) {
+  if (lane == 0) {
     __threadfence();
-    if (atomicAdd(p.sched + 3, 1u) == gridDim.x - 1) {
+    if (atomicAdd(p.sched + 3, 1u) == gridDim.x * kWarps - 1) {
       atomicExch(p.sched + 2, 0u);
       atomicExch(p.sched + 3, 0u);
     }
@@ -606,33 +683,18 @@ int pe_verify_sampled(const void* target_logits, const void* draft_logits, int d
   p.tail = V % epv;
   p.Rt = B * (Kp + 1);
   p.Rd = B * Kp;
-  // stats chunks: whole batches of kBatchVecs vectors, at most 4 per chunk,
-  // enough chunks for about one unit per CTA, at most the partial slots
-  int C = 1;
+  // stats units: at least kStatsChunkVecs vectors, at most kMaxChunksSampled
+  // per row; residual units: kResidChunkVecs vectors of each of two rows
+  int C = 1, C2 = 1;
   if (p.nvec > 0) {
-    const int nb = ceil_div(p.nvec, pe::kBatchVecs);
-    C = ceil_div(nb, 4);
-    const int want = ceil_div(grid_max, rows);
-    if (C < want) C = want;
-    const int c_max = ceil_div(p.nvec, pe::kThreads);
-    if (C > c_max) C = c_max;
-    if (C > pe::kMaxChunksSampled) C = pe::kMaxChunksSampled;
-    p.chunk_vecs = C <= nb ? ceil_div(nb, C) * pe::kBatchVecs : ceil_div(p.nvec, C);
+    p.chunk_vecs = ceil_div(p.nvec, pe::kMaxChunksSampled);
+    if (p.chunk_vecs < pe::kStatsChunkVecs) p.chunk_vecs = pe::kStatsChunkVecs;
     if (p.chunk_vecs > p.nvec) p.chunk_vecs = p.nvec;
     C = ceil_div(p.nvec, p.chunk_vecs);
-  }
-  p.C = C;
-  // residual chunks: about four units per CTA over all requests (those
-  // without a rejection leave at once)
-  int C2 = 1;
-  if (p.nvec > 0) {
-    C2 = ceil_div(4LL * grid_max, B);
-    const int c_max = ceil_div(p.nvec, pe::kThreads);
-    if (C2 > c_max) C2 = c_max;
-    if (C2 < 1) C2 = 1;
-    p.chunk2_vecs = ceil_div(p.nvec, C2);
+    p.chunk2_vecs = p.nvec < pe::kResidChunkVecs ? p.nvec : pe::kResidChunkVecs;
     C2 = ceil_div(p.nvec, p.chunk2_vecs);
   }
+  p.C = C;
   p.C2 = C2;
   if ((long long)B * C2 > 0x7fffffffLL || rows * C > 0x7fffffffLL) return PE_EINVAL;
   p.c2 = c2;
@@ -664,9 +726,11 @@ int pe_verify_sampled(const void* target_logits, const void* draft_logits, int d
   p.rkey = reinterpret_cast<unsigned long long*>(w + L.rkey_off);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const long long n1 = rows * p.C;
-  const int g1 = n1 < grid_max ? (int)n1 : grid_max;
-  const long long n2 = (long long)B * p.C2;
+  // persistent grids: 3 CTAs (24 warps) per SM, fewer for small problems
+  const long long n1 = ceil_div(rows * p.C, pe::kWarps);
+  const int g1_max = dev.sm_count * pe::kStatsCtasPerSm;
+  const int g1 = n1 < g1_max ? (int)n1 : g1_max;
+  const long long n2 = ceil_div((long long)B * p.C2, pe::kWarps);
   const int g2 = n2 < grid_max ? (int)n2 : grid_max;
   if (dtype == PE_BF16) {
     pe::sampled_stats_kernel<PE_BF16><<<g1, pe::kThreads, 0, st>>>(p);

@@ -892,26 +892,11 @@ void plan_argmax(pe::StepParams& p, int elt, int rows, int grid_max, int batches
   p.n_arg_units = rows * p.C;
 }
 
-// Dynamic shared memory above 48 KiB must be opted into once per kernel and
-// device (a host-side attribute; no synchronisation).
-template <class K>
-bool allow_smem(K kernel, int bytes, std::atomic<unsigned long long>& done_mask) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return false;
-  const unsigned long long bit = 1ull << dev;
-  if (done_mask.load(std::memory_order_relaxed) & bit) return true;
-  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
-      cudaSuccess)
-    return false;
-  done_mask.fetch_or(bit);
-  return true;
-}
-
 template <int DT, int STAGES, int MINB>
 int launch_tma(const pe::StepParams& p, int grid, cudaStream_t stream) {
   static std::atomic<unsigned long long> attr_done{0};
   const int smem = STAGES * pe::kStageBytes;
-  if (!allow_smem(pe::step_kernel_tma<DT, STAGES, MINB>, smem, attr_done)) return PE_ECUDA;
+  if (!pe_host::allow_smem(pe::step_kernel_tma<DT, STAGES, MINB>, smem, attr_done)) return PE_ECUDA;
   pe::step_kernel_tma<DT, STAGES, MINB><<<grid, pe::kTmaThreads, smem, stream>>>(p);
   return pe_host::launch_status();
 }

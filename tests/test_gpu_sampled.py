@@ -125,6 +125,8 @@ CASES = [
     ("first_draft_after_prefill_Kp0", 16, 0, 32000, torch.bfloat16, 1.0, 5),
     ("many_small_rows", 1000, 1, 64, torch.float32, 0.9, 6),
     ("f32_mid", 32, 7, 50000, torch.float32, 0.6, 7),
+    ("cold_T0.25", 64, 7, 32000, torch.bfloat16, 0.25, 10),
+    ("hot_T4_f32", 48, 5, 32003, torch.float32, 4.0, 11),
     ("decode_b64_V201088", 64, 7, 201088, torch.bfloat16, 1.0, 8),
     ("decode_b256_V151936", 256, 7, 151936, torch.bfloat16, 1.0, 9),
 ]
