@@ -171,6 +171,11 @@ struct Vec<PE_BF16> {
       z[2 * i + 1] = bf16_hi(w[i]);
     }
   }
+  // element e (a compile-time index after unrolling) of a vector
+  __device__ static __forceinline__ float elem(uint4 q, int e) {
+    const uint32_t w = (e >> 1) == 0 ? q.x : (e >> 1) == 1 ? q.y : (e >> 1) == 2 ? q.z : q.w;
+    return (e & 1) ? bf16_hi(w) : bf16_lo(w);
+  }
   // running maximum of raw values, two at a time
   __device__ static __forceinline__ uint32_t max_init() { return kNegInf; }
   __device__ static __forceinline__ uint32_t max_fold(uint32_t m, uint4 q) {
@@ -194,6 +199,9 @@ struct Vec<PE_F32> {
     z[1] = __uint_as_float(q.y);
     z[2] = __uint_as_float(q.z);
     z[3] = __uint_as_float(q.w);
+  }
+  __device__ static __forceinline__ float elem(uint4 q, int e) {
+    return __uint_as_float(e == 0 ? q.x : e == 1 ? q.y : e == 2 ? q.z : q.w);
   }
   __device__ static __forceinline__ uint32_t max_init() { return kNegInf; }
   __device__ static __forceinline__ uint32_t max_fold(uint32_t m, uint4 q) {
@@ -506,31 +514,31 @@ __device__ __forceinline__ void residual_unit(const SampledParams& p, int u, int
     const uint4* dr = reinterpret_cast<const uint4*>(drow);
     const int v_lo = c * p.chunk2_vecs;
     const int v_hi = min(v_lo + p.chunk2_vecs, p.nvec);
-    constexpr int kV = kVecPerThread / 2;  // two rows: half the vectors each
+    constexpr int kV = kVecPerThread / 4;  // two rows, and registers for the noise
     float thr = -INFINITY;  // best score of the warp so far (absolute log2 units)
     for (int base = v_lo; base < v_hi; base += 32 * kV) {
       const float K = ex2(thr) * kBound;  // d > K t: the column may beat thr
+      const bool whole = base + 32 * kV <= v_hi;  // no bounds to check
       uint4 xt[kV], xd[kV];
 #pragma unroll
       for (int i = 0; i < kV; ++i) {
         const int v = base + i * 32 + lane;
-        xt[i] = v < v_hi ? __ldcs(tr + v) : make_uint4(0u, 0u, 0u, 0u);
-        xd[i] = v < v_hi ? __ldcs(dr + v) : make_uint4(0u, 0u, 0u, 0u);
+        xt[i] = (whole || v < v_hi) ? __ldcs(tr + v) : make_uint4(0u, 0u, 0u, 0u);
+        xd[i] = (whole || v < v_hi) ? __ldcs(dr + v) : make_uint4(0u, 0u, 0u, 0u);
       }
 #pragma unroll
       for (int i = 0; i < kV; ++i) {
         const int v = base + i * 32 + lane;
-        if (v >= v_hi) continue;
-        float zt[E::kN], zd[E::kN];
-        E::unpack(xt[i], zt);
-        E::unpack(xd[i], zd);
+        if (!whole && v >= v_hi) continue;
 #pragma unroll
         for (int g = 0; g < E::kN / 4; ++g) {
           const uint4 w = philox(p, (uint32_t)((v * E::kN) / 4 + g), (uint32_t)b);
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             const int e = 4 * g + k;
-            const float d = ex2(fmaf(zt[e], p.c2, -Lt)) - ex2(fmaf(zd[e], p.c2, -Ld));
+            float at, ad;  // exponents of p and q, one packed instruction
+            fma2(at, ad, E::elem(xt[i], e), E::elem(xd[i], e), p.c2, p.c2, -Lt, -Ld);
+            const float d = ex2(at) - ex2(ad);
             const uint32_t wk = word(w, k);
             if (d > K * one_minus_u(wk)) {  // d > 0 and the column may beat thr
               const float sc = lg2(d) + noise2(wk);
@@ -588,7 +596,7 @@ __device__ __forceinline__ void residual_unit(const SampledParams& p, int u, int
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 3) sampled_residual_kernel(const SampledParams p) {
+__global__ void __launch_bounds__(kThreads, 4) sampled_residual_kernel(const SampledParams p) {
   const int lane = threadIdx.x & 31;
   const int n_units = p.B * p.C2;
   int u = 0;
@@ -672,7 +680,6 @@ int pe_verify_sampled(const void* target_logits, const void* draft_logits, int d
   if (!(c2 < 3.0e38f)) return PE_EINVAL;  // temperature so small that 1/T overflows
   pe_host::DeviceInfo dev;
   if (pe_host::device_info(&dev) != PE_OK) return PE_ECUDA;
-  const int grid_max = dev.sm_count * 3;
 
   pe::SampledParams p = {};
   p.B = B;
@@ -731,7 +738,7 @@ int pe_verify_sampled(const void* target_logits, const void* draft_logits, int d
   const int g1_max = dev.sm_count * pe::kStatsCtasPerSm;
   const int g1 = n1 < g1_max ? (int)n1 : g1_max;
   const long long n2 = ceil_div((long long)B * p.C2, pe::kWarps);
-  const int g2 = n2 < grid_max ? (int)n2 : grid_max;
+  const int g2 = n2 < g1_max ? (int)n2 : g1_max;
   if (dtype == PE_BF16) {
     pe::sampled_stats_kernel<PE_BF16><<<g1, pe::kThreads, 0, st>>>(p);
     pe::sampled_residual_kernel<PE_BF16><<<g2, pe::kThreads, 0, st>>>(p);
