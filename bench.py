@@ -42,6 +42,8 @@ FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("speculative_decoding_pe_gb300/csrc/pe_step.cu",
                   "speculative_decoding_pe_gb300/csrc/pe_internal.cuh",
                   "speculative_decoding_pe_gb300/csrc/pe_workspace.cuh")
+SAMPLED_SOURCES = ("speculative_decoding_pe_gb300/csrc/pe_sampled.cu",
+                   "speculative_decoding_pe_gb300/csrc/pe_internal.cuh")
 
 
 # ------------------------------------------------------------ distributed
@@ -132,25 +134,25 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload: str):
+def profiled_traffic(workload: str, kernel: str = "pe_step", sources=KERNEL_SOURCES):
     """DRAM bytes per launch from the committed ncu summary of this kernel and
     workload, or None when there is none or the kernel changed since."""
-    path = os.path.join(ROOT, "profiles", "pe_step_%s.md" % workload)
+    path = os.path.join(ROOT, "profiles", "%s_%s.md" % (kernel, workload))
     try:
         text = open(path).read()
     except OSError:
         return None
     m_hash = re.search(r"kernel_source_sha256_16\s*=\s*([0-9a-f]+)", text)
     m_bytes = re.search(r"dram_bytes_per_launch\s*=\s*([0-9]+)", text)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(sources):
         return None
     return int(m_bytes.group(1))
 
@@ -523,7 +525,10 @@ def run_sampled(args):
                        "min_us": min(step_ms) * 1e3},
             "us_per_step": mean_ms_max * 1e3,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
+                         "frac": achieved / peak,
+                         "traffic": profiled_traffic("decode_b256", "pe_verify_sampled",
+                                                     SAMPLED_SOURCES),
+                         "peak_source": peak_kind,
                          "algorithmic_bytes_per_launch": bytes_["total"],
                          "bytes": bytes_,
                          "kernel": "pe::sampled_stats_kernel + pe::sampled_residual_kernel "
