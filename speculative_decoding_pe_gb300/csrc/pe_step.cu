@@ -90,8 +90,6 @@ struct SharedState {
   int unit;
   int last;
   int first;
-  int skip2[2];  // early exit: unit is moot
-  int next2[2];  // early exit: next unit after a moot one
   int verdict[2];
   int amax[PE_MAX_KP + 1];
   int tok[PE_MAX_KP + 1];
@@ -415,12 +413,13 @@ __device__ __forceinline__ void finish_argmax_unit(const StepParams& p, SharedSt
 // Early exit reads a request's rows in order and stops after the first
 // mismatch.  Units run row-major over (row j, request b, chunk c), so every
 // request's row 0 streams first, then row 1, ...; a unit whose request is
-// already known to mismatch at an earlier row reads nothing.  The CTA that
-// completes a row records its argmax and ORs two bits into the request's
-// state word (row done; row's argmax equals the draft).  The OR after which
-// the rows 0..a are all done, 0..a-1 all match and a mismatches (or a = K')
-// settles the request: exactly one CTA sees that change, and it runs the
-// epilogue.  Nothing ever waits for another CTA.
+// already known to mismatch at an earlier row is skipped before it reads
+// anything (skip_moot).  The CTA that completes a row records its argmax and
+// ORs two bits into the request's state word (row done; row's argmax equals
+// the draft).  The OR after which the rows 0..a are all done, 0..a-1 all
+// match and a mismatches (or a = K') settles the request: exactly one CTA
+// sees that change, and it runs the epilogue.  Nothing ever waits for
+// another CTA.
 
 // Accepted length settled by a state word, or -1 while it is still open.
 __device__ __forceinline__ int settled(unsigned long long st, int Kp) {
@@ -440,7 +439,7 @@ __device__ __forceinline__ void argmax_unit_early(const StepParams& p, SharedSta
   const int rem = u - j * per_row;
   const int b = rem / p.C;
   const int c = rem - b * p.C;
-  const int r = b * (p.Kp + 1) + j;  // (moot units were skipped by the caller)
+  const int r = b * (p.Kp + 1) + j;  // (moot units were skipped by the scheduler)
   const char* rowp = logits_row(p, r);
   const int v_lo = c * p.chunk_vecs;
   const int v_hi = min(v_lo + p.chunk_vecs, p.nvec);
@@ -594,7 +593,7 @@ __device__ __forceinline__ void copy_tile(const StepParams& p, SharedState& sh, 
 }
 
 // ------------------------------------------------------------------- kernel
-template <int DT, bool EARLY>
+template <int DT>
 __global__ void __launch_bounds__(kThreads, 3) step_kernel(const StepParams p) {
   __shared__ SharedState sh;
   if (p.in_offsets && !offsets_valid(p.in_offsets, p.B, p.R, p.Kp + 1)) {
@@ -602,66 +601,87 @@ __global__ void __launch_bounds__(kThreads, 3) step_kernel(const StepParams p) {
     return;  // every CTA sees the same offsets and leaves without writing
   }
   // The first unit of each CTA is its own index; later units come from the
-  // counter, which therefore hands out gridDim.x + 0, 1, 2, ...
+  // counter, which therefore hands out gridDim.x + 0, 1, 2, ...  A CTA takes
+  // its next unit only when it is free: a unit handed out is a unit being
+  // read, so no request's last chunk waits behind another unit.
   int u = blockIdx.x;
-  int par = 0;
   while (u < p.n_units) {
-    unsigned next = 0;
-    if (threadIdx.x == 0) next = gridDim.x + atomicAdd(p.sched, 1u);  // prefetch
-    if (EARLY && u < p.n_arg_units && u >= p.B * p.C) {
-      // rows after row 0: moot once a mismatch is known at an earlier row.
-      // The state load and the next-unit fetch are in flight together; a
-      // moot unit costs one round trip and one barrier.
-      if (threadIdx.x == 0) {
-        const int per_row = p.B * p.C;
-        const int j = u / per_row;
-        const int b = (u - j * per_row) / p.C;
-        const unsigned long long st = __ldcg(p.state + b);
-        const unsigned done = (unsigned)st;
-        const unsigned match = (unsigned)(st >> 32);
-        const int moot = (done & ~match & ((1u << j) - 1u)) != 0u;
-        sh.skip2[par] = moot;
-        if (moot) sh.next2[par] = (int)next;
-      }
-      __syncthreads();
-      const int moot = sh.skip2[par];
-      const int nu = sh.next2[par];
-      par ^= 1;  // two slots: no thread is ever two barriers behind
-      if (moot) {
-        u = nu;
-        continue;
-      }
-    }
-    if (u < p.n_arg_units) {
-      if (EARLY)
-        argmax_unit_early<DT>(p, sh, u);
-      else
-        argmax_unit<DT>(p, sh, u);
-    } else
+    if (u < p.n_arg_units)
+      argmax_unit<DT>(p, sh, u);
+    else
       copy_tile<SyncAll>(p, sh, u - p.n_arg_units);
     __syncthreads();
-    if (threadIdx.x == 0) sh.unit = (int)next;
+    if (threadIdx.x == 0) sh.unit = (int)(gridDim.x + atomicAdd(p.sched, 1u));
     __syncthreads();
     u = sh.unit;
   }
   if (threadIdx.x == 0) {
     __threadfence();
-    const unsigned done = atomicAdd(p.sched + 1, 1u);
-    sh.last = done == gridDim.x - 1;  // every other CTA has left
-    if (sh.last) {
+    if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {  // every other CTA has left
       atomicExch(p.sched, 0u);
       atomicExch(p.sched + 1, 0u);
     }
   }
-  if (EARLY) {  // the last CTA clears partly read rows and the row results
+}
+
+// --------------------------------------------------- early-exit scheduling
+// Units are handed out in order (argmax units row-major, then copy tiles).
+// A CTA takes its next unit only when it is free (a unit handed out is a
+// unit being read, so rows complete, and their requests' verdicts become
+// known, as early as possible); thread 0 checks the unit's request and, if
+// it is already known to mismatch at an earlier row, takes the next index
+// instead, alone, without holding the CTA at a barrier per skipped unit.
+
+// First unit at or after claim u that is worth reading (thread 0 only).
+__device__ __forceinline__ int skip_moot(const StepParams& p, int u) {
+  const int per_row = p.B * p.C;
+  while (u < p.n_arg_units) {
+    const int j = u / per_row;
+    if (j == 0) return u;
+    const int b = (u - j * per_row) / p.C;
+    const unsigned long long st = __ldcg(p.state + b);
+    const unsigned done = (unsigned)st, match = (unsigned)(st >> 32);
+    if (!(done & ~match & ((1u << j) - 1u))) return u;  // no earlier mismatch known
+    u = (int)atomicAdd(p.sched, 1u);                    // moot: take the next one
+  }
+  return u;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 3) step_kernel_early(const StepParams p) {
+  __shared__ SharedState sh;
+  if (p.in_offsets && !offsets_valid(p.in_offsets, p.B, p.R, p.Kp + 1)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.err, PE_ERR_OFFSETS);
+    return;  // every CTA sees the same offsets and leaves without writing
+  }
+  for (;;) {
+    if (threadIdx.x == 0) sh.unit = skip_moot(p, (int)atomicAdd(p.sched, 1u));
     __syncthreads();
-    if (sh.last) {
-      for (int i = threadIdx.x; i < p.Rl; i += kThreads) {
-        p.keys[i] = 0ull;
-        p.rcount[i] = 0u;
-        p.amax_ws[i] = 0;
-      }
-      for (int i = threadIdx.x; i < p.B; i += kThreads) p.state[i] = 0ull;
+    const int u = sh.unit;
+    if (u >= p.n_units) break;
+    if (u < p.n_arg_units)
+      argmax_unit_early<DT>(p, sh, u);
+    else
+      copy_tile<SyncAll>(p, sh, u - p.n_arg_units);
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned done = atomicAdd(p.sched + 1, 1u);
+    sh.last = done == gridDim.x - 1;  // every other CTA has left
+  }
+  __syncthreads();
+  if (sh.last) {  // the last CTA clears partly read rows, states and row results
+    __threadfence();
+    for (int i = threadIdx.x; i < p.Rl; i += kThreads) {
+      p.keys[i] = 0ull;
+      p.rcount[i] = 0u;
+      p.amax_ws[i] = 0;
+    }
+    for (int i = threadIdx.x; i < p.B; i += kThreads) p.state[i] = 0ull;
+    if (threadIdx.x == 0) {
+      atomicExch(p.sched, 0u);
+      atomicExch(p.sched + 1, 0u);
     }
   }
 }
@@ -921,17 +941,17 @@ int launch(const pe::StepParams& p, int dtype, int grid, const pe_host::Tuning& 
                : launch_tma<PE_F32, 12, 1>(p, grid, stream);
   }
   if (dtype == PE_BF16)
-    pe::step_kernel<PE_BF16, false><<<grid, pe::kThreads, 0, stream>>>(p);
+    pe::step_kernel<PE_BF16><<<grid, pe::kThreads, 0, stream>>>(p);
   else
-    pe::step_kernel<PE_F32, false><<<grid, pe::kThreads, 0, stream>>>(p);
+    pe::step_kernel<PE_F32><<<grid, pe::kThreads, 0, stream>>>(p);
   return pe_host::launch_status();
 }
 
 int launch_early(const pe::StepParams& p, int dtype, int grid, cudaStream_t stream) {
   if (dtype == PE_BF16)
-    pe::step_kernel<PE_BF16, true><<<grid, pe::kThreads, 0, stream>>>(p);
+    pe::step_kernel_early<PE_BF16><<<grid, pe::kThreads, 0, stream>>>(p);
   else
-    pe::step_kernel<PE_F32, true><<<grid, pe::kThreads, 0, stream>>>(p);
+    pe::step_kernel_early<PE_F32><<<grid, pe::kThreads, 0, stream>>>(p);
   return pe_host::launch_status();
 }
 
