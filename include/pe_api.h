@@ -307,6 +307,14 @@ typedef struct pe_tuning {
   int32_t chunk_batches;   /* max 32 KiB load batches per argmax unit      */
   int32_t rows_per_unit;   /* X rows per copy unit                         */
   int32_t variant;         /* 1: register streaming, 2: bulk-copy pipeline */
+  int32_t queue_order;     /* 2: argmax chunks first, every copy tile after
+                              (default: the tiles fill the drain, and a
+                              request's last verified-row tile, not its
+                              verdict, usually writes the bonus row);
+                              1: copy tiles of the verified rows first, then
+                              the argmax chunks, then the other copy tiles
+                              (same outputs; the verdict usually writes the
+                              bonus row) */
 } pe_tuning;
 int pe_get_tuning(pe_tuning* out /* host */);
 int pe_set_tuning(const pe_tuning* in /* host */);

@@ -11,10 +11,11 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];  // 0 = not queried yet
 
-std::atomic<int> g_ctas_per_sm{3};
-std::atomic<int> g_chunk_batches{4};
-std::atomic<int> g_rows_per_unit{8};
+std::atomic<int> g_ctas_per_sm{4};
+std::atomic<int> g_chunk_batches{3};
+std::atomic<int> g_rows_per_unit{4};
 std::atomic<int> g_variant{1};
+std::atomic<int> g_queue_order{2};
 }  // namespace
 
 int device_info(DeviceInfo* out) {
@@ -38,6 +39,7 @@ Tuning tuning() {
   t.chunk_batches = g_chunk_batches.load(std::memory_order_relaxed);
   t.rows_per_unit = g_rows_per_unit.load(std::memory_order_relaxed);
   t.variant = g_variant.load(std::memory_order_relaxed);
+  t.queue_order = g_queue_order.load(std::memory_order_relaxed);
   return t;
 }
 
@@ -57,6 +59,7 @@ int pe_get_tuning(pe_tuning* out) {
   out->chunk_batches = t.chunk_batches;
   out->rows_per_unit = t.rows_per_unit;
   out->variant = t.variant;
+  out->queue_order = t.queue_order;
   return PE_OK;
 }
 
@@ -67,10 +70,12 @@ int pe_set_tuning(const pe_tuning* in) {
   if (in->rows_per_unit < 0 || in->rows_per_unit > pe::kMaxRowsPerUnit)
     return PE_EINVAL;
   if (in->variant < 0 || in->variant > 2) return PE_EINVAL;
+  if (in->queue_order < 0 || in->queue_order > 2) return PE_EINVAL;
   if (in->ctas_per_sm) pe_host::g_ctas_per_sm.store(in->ctas_per_sm);
   if (in->chunk_batches) pe_host::g_chunk_batches.store(in->chunk_batches);
   if (in->rows_per_unit) pe_host::g_rows_per_unit.store(in->rows_per_unit);
   if (in->variant) pe_host::g_variant.store(in->variant);
+  if (in->queue_order) pe_host::g_queue_order.store(in->queue_order);
   return PE_OK;
 }
 

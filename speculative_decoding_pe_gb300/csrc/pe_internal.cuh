@@ -100,6 +100,7 @@ struct Tuning {
   int chunk_batches;
   int rows_per_unit;
   int variant;
+  int queue_order;
 };
 Tuning tuning();
 

@@ -52,6 +52,8 @@ struct StepParams {
   int nvec, tail;         // whole 16-byte vectors per logits row, leftover elements
   int chunk_vecs, C, Rl;  // argmax chunking: vectors per chunk, chunks per row, rows
   int n_arg_units, rows_per_unit, n_copy_units, n_units;
+  int rv, n_vtile;        // verified rows B(K'+1); copy tiles over them
+  int vfirst;             // 1: those tiles are handed out before the argmax chunks
   const void* logits;
   const int32_t* row_index;  // logits row of argmax row r (NULL: r itself)
   int rows_total;            // logits rows addressable through row_index
@@ -78,6 +80,7 @@ struct StepParams {
   uint32_t* count;
   unsigned long long* keys;
   unsigned long long* state;  // early exit: per-request done / match bits
+  unsigned long long* xfer;   // per-request bonus-row hand-off word
   uint32_t* rcount;           // early exit: finished chunks per row
   int32_t* amax_ws;           // early exit: argmax of each completed row
   uint32_t* err;
@@ -97,7 +100,32 @@ struct SharedState {
   const uint4* src[2 * kMaxRowsPerUnit];
   uint4* dst[2 * kMaxRowsPerUnit];
   int mode[2 * kMaxRowsPerUnit];
+  int vreq[kMaxRowsPerUnit];   // copy tile: request of each verified row
+  int vrow0[kMaxRowsPerUnit];  // ... and the X row of its verified slot 0
+  int nbonus;                  // bonus rows this tile writes
+  int brow[kMaxRowsPerUnit];
+  int btok[kMaxRowsPerUnit];
+  int xwrite;                  // epilogue: this verdict writes the bonus row
 };
+
+// Hand-off word of a request (workspace xfer[b]): verified rows whose
+// default embedding half a copy tile has written (bits 0-15), verdict taken
+// (bit 16), accepted length (bits 17-24), bonus token (bits 32-63).
+constexpr unsigned long long kXferCount = 0xffffull;
+constexpr unsigned long long kXferVerdict = 1ull << 16;
+
+// Unit handed out at position q of the queue.  vfirst: the copy tiles of
+// the verified rows first, then the argmax chunks, then the other copy tiles
+// (prompt and MASK rows), so that a verified row's default embedding half is
+// normally written before its request's verdict.  Otherwise (the default,
+// measured faster): the argmax chunks, then every copy tile, which fill the
+// drain at the end of the step.
+__device__ __forceinline__ int unit_at(const StepParams& p, int q) {
+  if (!p.vfirst) return q;  // argmax chunks, then every copy tile
+  if (q < p.n_vtile) return p.n_arg_units + q;
+  if (q < p.n_vtile + p.n_arg_units) return q - p.n_vtile;
+  return q;
+}
 
 // Logits row read for argmax row r, or nullptr when an index given through
 // row_index is outside [0, rows_total).
@@ -109,28 +137,6 @@ __device__ __forceinline__ const char* logits_row(const StepParams& p, int r) {
 
 __device__ __forceinline__ int seg_begin(const StepParams& p, int b) {
   return p.in_offsets ? __ldg(p.in_offsets + b) : b * (p.Kp + 1);
-}
-
-// Segment (request b, its input offset io and length n) of output row t.
-__device__ __forceinline__ void locate(const StepParams& p, int t, int& b, int& io,
-                                       int& n) {
-  if (!p.in_offsets) {
-    b = t / (p.Kp + p.K);
-    io = b * (p.Kp + 1);
-    n = p.Kp + 1;
-    return;
-  }
-  int lo = 0, hi = p.B - 1;  // largest b with oo_b = io_b + b(K-1) <= t
-  while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (__ldg(p.in_offsets + mid) + mid * (p.K - 1) <= t)
-      lo = mid;
-    else
-      hi = mid - 1;
-  }
-  b = lo;
-  io = __ldg(p.in_offsets + b);
-  n = __ldg(p.in_offsets + b + 1) - io;
 }
 
 // ------------------------------------------------------------ element types
@@ -247,31 +253,33 @@ __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedStat
   // shifted draft d_{j+1} elsewhere, and the MASK id in the last row when it
   // is rejected.
   auto slot_token = [&](int j) { return j == a ? bonus : (j < Kp ? sh.tok[j] : p.mask_id); };
-  // embedding half of the verified rows
-  const int total = nr * p.nvh;
-  for (int q0 = 0; q0 < total; q0 += kBatchVecs) {
-    uint4 v[kVecPerThread];
-    long long dst[kVecPerThread];
-#pragma unroll
-    for (int i = 0; i < kVecPerThread; ++i) {
-      const int q = q0 + i * kThreads + tid;
-      dst[i] = -1;
-      if (q < total) {
-        const int j = q / p.nvh;
-        const int c = q - j * p.nvh;
-        const int tok = slot_token(j);
-        dst[i] = (long long)(oo + vb + j) * 2 * p.nvh + c;
-        if (tok >= 0 && tok < p.V) {
-          v[i] = __ldg(p.emb + (long long)tok * p.nvh + c);
-        } else {
-          v[i] = make_uint4(0u, 0u, 0u, 0u);
-          if (c == 0) atomicOr(p.err, PE_ERR_TOKEN_RANGE);
-        }
-      }
+  // Embedding halves of the verified rows: the copy tiles write each one
+  // with the token it has unless it is the bonus slot; only the bonus row
+  // depends on the verdict, and whichever of this verdict and the request's
+  // last verified-row tile comes second writes it (one atomic each on the
+  // request's hand-off word).  Tokens outside the table give zero halves
+  // (written by the tiles) and an error bit (raised here).
+  if (tid < nr) {
+    const int tok = slot_token(tid);
+    if (tok < 0 || tok >= p.V) atomicOr(p.err, PE_ERR_TOKEN_RANGE);
+  }
+  if (tid == 0) {
+    const unsigned long long old = atomicOr(
+        p.xfer + b,
+        kXferVerdict | ((unsigned long long)a << 17) | ((unsigned long long)(uint32_t)bonus << 32));
+    const bool mine = (old & kXferCount) == (unsigned long long)nr;
+    if (mine) {
+      atomicExch(p.xfer + b, 0ull);  // both sides are done: clear for the next call
+      __threadfence();
     }
-#pragma unroll
-    for (int i = 0; i < kVecPerThread; ++i)
-      if (dst[i] >= 0) p.X[dst[i]] = v[i];
+    sh.xwrite = mine ? 1 : 0;
+  }
+  S::sync();
+  if (sh.xwrite) {
+    uint4* dst = p.X + (long long)(oo + s) * 2 * p.nvh;
+    const bool ok = bonus >= 0 && bonus < p.V;
+    for (int v = tid; v < p.nvh; v += kThreads)
+      dst[v] = ok ? __ldg(p.emb + (long long)bonus * p.nvh + v) : make_uint4(0u, 0u, 0u, 0u);
   }
   // rebuild metadata of the verified rows (j <= Kp) and MASK rows (j > Kp)
   for (int j = tid; j < Kp + p.K; j += kThreads) {
@@ -501,15 +509,57 @@ __device__ __forceinline__ void argmax_unit_early(const StepParams& p, SharedSta
 // ------------------------------------------------------------------ X tiles
 // Rows whose content verification cannot change: hidden half of every row,
 // MASK rows entirely, prompt rows (prefill) entirely plus their metadata.
+// X row t (request b, segment io / n) of row i of the verified rows, which
+// are listed request by request, K'+1 each.
+__device__ __forceinline__ void verified_row(const StepParams& p, int i, int& t, int& b,
+                                             int& io, int& n) {
+  const int nr = p.Kp + 1;
+  b = i / nr;
+  io = seg_begin(p, b);
+  n = seg_begin(p, b + 1) - io;
+  t = io + b * (p.K - 1) + (n - nr) + (i - b * nr);
+}
+
+// X row t of row i of the other rows: each request's prompt rows, then its
+// K-1 MASK rows, request by request; request b holds n_b - (K'+1) + K - 1
+// of them, starting at oo_b - b(K'+1).
+__device__ __forceinline__ void other_row(const StepParams& p, int i, int& t, int& b, int& io,
+                                          int& n) {
+  const int nr = p.Kp + 1;
+  if (!p.in_offsets) {  // decode: MASK rows only (K > 1 when there are any)
+    b = i / (p.K - 1);
+    io = b * nr;
+    n = nr;
+    t = io + b * (p.K - 1) + nr + (i - b * (p.K - 1));
+    return;
+  }
+  int lo = 0, hi = p.B - 1;  // largest b whose first such row is at or before i
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (__ldg(p.in_offsets + mid) + mid * (p.K - 1 - nr) <= i)
+      lo = mid;
+    else
+      hi = mid - 1;
+  }
+  b = lo;
+  io = __ldg(p.in_offsets + b);
+  n = __ldg(p.in_offsets + b + 1) - io;
+  const int l = i - (io + b * (p.K - 1 - nr));
+  t = io + b * (p.K - 1) + (l < n - nr ? l : l + nr);
+}
+
 template <class S, int kSeg, int kCols>
 __device__ __forceinline__ void copy_unit(const StepParams& p, SharedState& sh, int u) {
   const int tid = threadIdx.x;
-  const int t0 = u * p.rows_per_unit;
-  const int nrows = min(p.rows_per_unit, p.T - t0);
+  const bool vtile = u < p.n_vtile;  // a tile of verified rows
+  const int i0 = (vtile ? u : u - p.n_vtile) * p.rows_per_unit;
+  const int nrows = min(p.rows_per_unit, (vtile ? p.rv : p.T - p.rv) - i0);
   if (tid < nrows) {
-    const int t = t0 + tid;
-    int b, io, n;
-    locate(p, t, b, io, n);
+    int t, b, io, n;
+    if (vtile)
+      verified_row(p, i0 + tid, t, b, io, n);
+    else
+      other_row(p, i0 + tid, t, b, io, n);
     const int oo = io + b * (p.K - 1);
     const int k = t - oo;
     const int vb = n - 1 - p.Kp;
@@ -534,9 +584,23 @@ __device__ __forceinline__ void copy_unit(const StepParams& p, SharedState& sh, 
         atomicOr(p.err, PE_ERR_TOKEN_RANGE);
       }
       sh_src = p.hidden + (long long)(io + k) * p.nvh;
-    } else if (k < n) {  // verified row: its embedding half waits for the bonus
-      me = kSkip;
+    } else if (k < n) {
+      // verified slot j: the token it has unless it is the bonus slot (the
+      // shifted draft d_{j+1}, or the MASK id in the last row); the bonus
+      // row is rewritten through the request's hand-off word.  A token
+      // outside the table gives a zero half here; the verdict raises the
+      // error bit for the slots that keep it.
+      const int j = k - vb;
+      const int tok = j < p.Kp ? __ldg(p.in_tokens + io + k + 1) : p.mask_id;
+      if (tok >= 0 && tok < p.V) {
+        me = kCopy;
+        se = p.emb + (long long)tok * p.nvh;
+      } else {
+        me = kZero;
+      }
       sh_src = p.hidden + (long long)(io + k) * p.nvh;
+      sh.vreq[tid] = b;
+      sh.vrow0[tid] = oo + vb;
     } else {  // MASK row: emb(mask) (+) h_shared
       me = kCopy;
       se = p.emb + (long long)p.mask_id * p.nvh;
@@ -549,6 +613,7 @@ __device__ __forceinline__ void copy_unit(const StepParams& p, SharedState& sh, 
     sh.src[2 * tid + 1] = sh_src;
     sh.dst[2 * tid + 1] = xr + p.nvh;
   }
+  if (tid == 0) sh.nbonus = 0;
   S::sync();
   const int nseg = 2 * nrows;  // kSeg half rows x kCols vectors per thread per batch
   for (int v0 = 0; v0 < p.nvh; v0 += kCols * kThreads) {
@@ -579,6 +644,34 @@ __device__ __forceinline__ void copy_unit(const StepParams& p, SharedState& sh, 
       }
     }
   }
+  if (!vtile) return;
+  // Hand-off: count this tile's verified rows into their requests' words,
+  // after every thread's stores of the tile are visible device-wide.  The
+  // tile that completes a request's count after its verdict was taken
+  // writes the bonus row (its embedding half with the bonus token); if the
+  // verdict comes later, the verdict writes it.
+  __threadfence();
+  S::sync();
+  if (tid < nrows) {
+    const int b = sh.vreq[tid];
+    const unsigned long long old = atomicAdd(p.xfer + b, 1ull);
+    if ((old & kXferCount) + 1 == (unsigned long long)(p.Kp + 1) && (old & kXferVerdict)) {
+      atomicExch(p.xfer + b, 0ull);  // both sides are done: clear for the next call
+      __threadfence();
+      const int e = atomicAdd(&sh.nbonus, 1);
+      sh.brow[e] = sh.vrow0[tid] + (int)((old >> 17) & 0xffull);
+      sh.btok[e] = (int)(uint32_t)(old >> 32);
+    }
+  }
+  S::sync();
+  const int nb = sh.nbonus;
+  for (int e = 0; e < nb; ++e) {
+    const int tok = sh.btok[e];
+    uint4* dst = p.X + (long long)sh.brow[e] * 2 * p.nvh;
+    const bool ok = tok >= 0 && tok < p.V;
+    for (int v = tid; v < p.nvh; v += kThreads)
+      dst[v] = ok ? __ldg(p.emb + (long long)tok * p.nvh + v) : make_uint4(0u, 0u, 0u, 0u);
+  }
 }
 
 // Copy tile with eight loads per thread in flight: eight half rows at a time
@@ -594,7 +687,7 @@ __device__ __forceinline__ void copy_tile(const StepParams& p, SharedState& sh, 
 
 // ------------------------------------------------------------------- kernel
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 3) step_kernel(const StepParams p) {
+__global__ void __launch_bounds__(kThreads, 4) step_kernel(const StepParams p) {
   __shared__ SharedState sh;
   if (p.in_offsets && !offsets_valid(p.in_offsets, p.B, p.R, p.Kp + 1)) {
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.err, PE_ERR_OFFSETS);
@@ -604,8 +697,9 @@ __global__ void __launch_bounds__(kThreads, 3) step_kernel(const StepParams p) {
   // counter, which therefore hands out gridDim.x + 0, 1, 2, ...  A CTA takes
   // its next unit only when it is free: a unit handed out is a unit being
   // read, so no request's last chunk waits behind another unit.
-  int u = blockIdx.x;
-  while (u < p.n_units) {
+  int q = blockIdx.x;  // queue position; unit_at gives the unit
+  while (q < p.n_units) {
+    const int u = unit_at(p, q);
     if (u < p.n_arg_units)
       argmax_unit<DT>(p, sh, u);
     else
@@ -613,7 +707,7 @@ __global__ void __launch_bounds__(kThreads, 3) step_kernel(const StepParams p) {
     __syncthreads();
     if (threadIdx.x == 0) sh.unit = (int)(gridDim.x + atomicAdd(p.sched, 1u));
     __syncthreads();
-    u = sh.unit;
+    q = sh.unit;
   }
   if (threadIdx.x == 0) {
     __threadfence();
@@ -632,23 +726,26 @@ __global__ void __launch_bounds__(kThreads, 3) step_kernel(const StepParams p) {
 // it is already known to mismatch at an earlier row, takes the next index
 // instead, alone, without holding the CTA at a barrier per skipped unit.
 
-// First unit at or after claim u that is worth reading (thread 0 only).
-__device__ __forceinline__ int skip_moot(const StepParams& p, int u) {
+// Unit at or after queue position q that is worth reading, or a value
+// >= n_units when the queue is exhausted (thread 0 only).
+__device__ __forceinline__ int skip_moot(const StepParams& p, int q) {
   const int per_row = p.B * p.C;
-  while (u < p.n_arg_units) {
+  while (q < p.n_units) {
+    const int u = unit_at(p, q);
+    if (u >= p.n_arg_units) return u;  // copy tile
     const int j = u / per_row;
     if (j == 0) return u;
     const int b = (u - j * per_row) / p.C;
     const unsigned long long st = __ldcg(p.state + b);
     const unsigned done = (unsigned)st, match = (unsigned)(st >> 32);
     if (!(done & ~match & ((1u << j) - 1u))) return u;  // no earlier mismatch known
-    u = (int)atomicAdd(p.sched, 1u);                    // moot: take the next one
+    q = (int)atomicAdd(p.sched, 1u);                    // moot: take the next one
   }
-  return u;
+  return p.n_units;
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 3) step_kernel_early(const StepParams p) {
+__global__ void __launch_bounds__(kThreads, 4) step_kernel_early(const StepParams p) {
   __shared__ SharedState sh;
   if (p.in_offsets && !offsets_valid(p.in_offsets, p.B, p.R, p.Kp + 1)) {
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.err, PE_ERR_OFFSETS);
@@ -715,9 +812,10 @@ __device__ __forceinline__ void produce(const StepParams& p, uint4* ring, uint64
   int pend[STAGES];  // parity of the last phase a copy was issued for, or -1
 #pragma unroll
   for (int s = 0; s < STAGES; ++s) pend[s] = -1;
-  int u = blockIdx.x;
+  int q = blockIdx.x;  // queue position; unit_at gives the unit
   for (;;) {
-    const bool stop = u >= p.n_units;
+    const bool stop = q >= p.n_units;
+    const int u = stop ? p.n_units : unit_at(p, q);
     const int next = stop ? 0 : (int)(gridDim.x + atomicAdd(p.sched, 1u));
     if (stop || u >= p.n_arg_units) {
       if (!(ok = mbar_wait(&empty[stage], phase ^ 1))) break;
@@ -758,7 +856,7 @@ __device__ __forceinline__ void produce(const StepParams& p, uint4* ring, uint64
       } while (v < v_hi);
       if (!ok) break;
     }
-    u = next;
+    q = next;
   }
   if (!ok) {
     atomicOr(p.err, PE_ERR_TIMEOUT);
@@ -961,6 +1059,7 @@ void bind_workspace(pe::StepParams& p, void* ws, int rows, int B) {
   p.sched = reinterpret_cast<uint32_t*>(base);
   p.count = reinterpret_cast<uint32_t*>(base + L.count_off);
   p.state = reinterpret_cast<unsigned long long*>(base + L.state_off);
+  p.xfer = reinterpret_cast<unsigned long long*>(base + L.xfer_off);
   p.keys = reinterpret_cast<unsigned long long*>(base + L.key_off);
   p.rcount = reinterpret_cast<uint32_t*>(base + L.rcount_off);
   p.amax_ws = reinterpret_cast<int32_t*>(base + L.amax_off);
@@ -1142,7 +1241,10 @@ int step_common(const pe_step_args* a, void* stream, bool early) {
   const int grid_max = grid_max_for(tk, dev);
   plan_argmax(p, elt, rows, grid_max, tk.chunk_batches);
   p.rows_per_unit = tk.rows_per_unit;
-  p.n_copy_units = (p.T + p.rows_per_unit - 1) / p.rows_per_unit;
+  p.rv = rows;  // verified rows: tiles of their own
+  p.n_vtile = (p.rv + p.rows_per_unit - 1) / p.rows_per_unit;
+  p.vfirst = tk.queue_order != 2;
+  p.n_copy_units = p.n_vtile + (p.T - p.rv + p.rows_per_unit - 1) / p.rows_per_unit;
   p.n_units = p.n_arg_units + p.n_copy_units;
   bind_workspace(p, a->workspace, rows, B);
   const int grid = p.n_units < grid_max ? p.n_units : grid_max;

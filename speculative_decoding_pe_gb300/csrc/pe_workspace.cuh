@@ -5,13 +5,19 @@
 //   [8]   uint32 count[B]      finished argmax units per request
 //   [..]  uint64 state[B]      early exit: rows done (bits 0-31) and rows
 //                              whose argmax matched the draft (bits 32-63)
+//   [..]  uint64 xfer[B]       bonus-row hand-off between the copy tiles and
+//                              the request's verdict: verified rows whose
+//                              default embedding half is written (bits
+//                              0-15), verdict known (bit 16), accepted
+//                              length (bits 17-24), bonus token (bits 32-63)
 //   [..]  uint64 key[rows]     running (value, column) maximum per logits row
 //   [..]  uint32 rcount[rows]  early exit: finished chunks per row
 //   [..]  int32  amax[rows]    early exit: argmax of each completed row
 //
 // Every field is zero between calls, so one workspace serves calls of any
 // size up to the one it was sized for: the full step clears a request's keys
-// and count when its last unit arrives, the early-exit step clears completed
+// and count when its last unit arrives, and its hand-off word when the
+// bonus row is written, the early-exit step clears completed
 // rows as they complete and everything else (partly read rows, states, row
 // results) in its last CTA; the last CTA to leave clears the two scheduler
 // words.
@@ -23,11 +29,12 @@
 namespace pe {
 
 struct WorkspaceLayout {
-  size_t count_off, state_off, key_off, rcount_off, amax_off, bytes;
+  size_t count_off, state_off, xfer_off, key_off, rcount_off, amax_off, bytes;
   WorkspaceLayout(int64_t rows, int64_t B) {
     count_off = 8;
     state_off = (count_off + 4 * (size_t)B + 7) & ~(size_t)7;
-    key_off = state_off + 8 * (size_t)B;
+    xfer_off = state_off + 8 * (size_t)B;
+    key_off = xfer_off + 8 * (size_t)B;
     rcount_off = key_off + 8 * (size_t)rows;
     amax_off = rcount_off + 4 * (size_t)rows;
     bytes = (amax_off + 4 * (size_t)rows + 255) & ~(size_t)255;

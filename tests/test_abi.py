@@ -157,5 +157,9 @@ def test_tuning_roundtrip(lib):
         assert t["chunk_batches"] == before["chunk_batches"]
         with pytest.raises(_native.PEError):
             _native.set_tuning(rows_per_unit=17)
+        with pytest.raises(_native.PEError):
+            _native.set_tuning(queue_order=3)
+        _native.set_tuning(queue_order=2)
+        assert _native.get_tuning()["queue_order"] == 2
     finally:
         _native.set_tuning(**before)

@@ -74,6 +74,24 @@ def test_early_exit_variants(spec):
         check_early(w, got, oracle_of(w))
 
 
+@pytest.mark.parametrize("queue_order", [1, 2], ids=["tiles_first", "tiles_last"])
+def test_early_exit_queue_orders(queue_order):
+    """Either order of copy tiles and argmax chunks gives the same outputs:
+    the bonus row is written by the verdict or by the request's last
+    verified-row tile, whichever comes second."""
+    before = _native.get_tuning()
+    try:
+        _native.set_tuning(queue_order=queue_order, rows_per_unit=3)
+        for spec, seed in ((wl.SPECS["decode_b256"].with_(B=48, V=30011, row_pad=5), 11),
+                           (wl.SPECS["decode_b64"].with_(B=16, V=20011, row_pad=5), 12)):
+            w = wl.make_workload(spec, seed, device="cuda")
+            got, ws = run_early(w)
+            check_early(w, got, oracle_of(w))
+            assert int(ws.count_nonzero()) == 0
+    finally:
+        _native.set_tuning(**before)
+
+
 def test_workspace_shared_with_full_step():
     """Early-exit and full steps alternate on one workspace; each leaves it
     clean for the other."""

@@ -45,8 +45,9 @@ class tuned:
         _native.set_tuning(**self.before)
 
 
-VARIANTS = [dict(variant=1), dict(variant=2)]
-VARIANT_IDS = ["regs", "pipeline"]
+VARIANTS = [dict(variant=1), dict(variant=2), dict(variant=1, queue_order=2),
+            dict(variant=2, queue_order=2)]
+VARIANT_IDS = ["regs", "pipeline", "regs_tiles_last", "pipeline_tiles_last"]
 
 
 # ------------------------------------------------------------ full sizes
@@ -113,6 +114,9 @@ def test_fused_step_variants(spec, variant):
                                          rows_per_unit=16),
                                     dict(variant=2, ctas_per_sm=2, chunk_batches=16,
                                          rows_per_unit=1),
+                                    dict(queue_order=2, rows_per_unit=1),
+                                    dict(queue_order=2, ctas_per_sm=1, rows_per_unit=16),
+                                    dict(ctas_per_sm=3),
                                     ],
                          ids=lambda d: ",".join("%s=%d" % kv for kv in d.items()) or "default")
 def test_launch_shapes_do_not_change_results(tuning):
