@@ -1001,9 +1001,12 @@ void plan_argmax(pe::StepParams& p, int elt, int rows, int grid_max, int batches
     int C = c_min > c_want ? c_min : c_want;
     if (C > c_max) C = c_max;
     if (C < 1) C = 1;
+    // Chunks of whole batches (only a row's last chunk is ragged; measured
+    // faster than equal chunks with a partial last batch each), or, below
+    // one batch, of whole vectors per thread.
     int chunk = (p.nvec + C - 1) / C;
-    if (chunk > pe::kBatchVecs)  // whole batches, so only a row's last chunk is ragged
-      chunk = (chunk + pe::kBatchVecs - 1) / pe::kBatchVecs * pe::kBatchVecs;
+    const int grain = chunk > pe::kBatchVecs ? pe::kBatchVecs : pe::kThreads;
+    chunk = (chunk + grain - 1) / grain * grain;
     p.chunk_vecs = chunk;
     p.C = (p.nvec + chunk - 1) / chunk;
   }
