@@ -259,28 +259,17 @@ __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedStat
   // last verified-row tile comes second writes it (one atomic each on the
   // request's hand-off word).  Tokens outside the table give zero halves
   // (written by the tiles) and an error bit (raised here).
+  // The hand-off atomic, the block-table loads of the metadata and (when
+  // this verdict writes it) the bonus row's loads are independent, so they
+  // share round trips.
   if (tid < nr) {
     const int tok = slot_token(tid);
     if (tok < 0 || tok >= p.V) atomicOr(p.err, PE_ERR_TOKEN_RANGE);
   }
-  if (tid == 0) {
-    const unsigned long long old = atomicOr(
-        p.xfer + b,
-        kXferVerdict | ((unsigned long long)a << 17) | ((unsigned long long)(uint32_t)bonus << 32));
-    const bool mine = (old & kXferCount) == (unsigned long long)nr;
-    if (mine) {
-      atomicExch(p.xfer + b, 0ull);  // both sides are done: clear for the next call
-      __threadfence();
-    }
-    sh.xwrite = mine ? 1 : 0;
-  }
-  S::sync();
-  if (sh.xwrite) {
-    uint4* dst = p.X + (long long)(oo + s) * 2 * p.nvh;
-    const bool ok = bonus >= 0 && bonus < p.V;
-    for (int v = tid; v < p.nvh; v += kThreads)
-      dst[v] = ok ? __ldg(p.emb + (long long)bonus * p.nvh + v) : make_uint4(0u, 0u, 0u, 0u);
-  }
+  unsigned long long old = 0ull;
+  if (tid == 0)
+    old = atomicOr(p.xfer + b, kXferVerdict | ((unsigned long long)a << 17) |
+                                   ((unsigned long long)(uint32_t)bonus << 32));
   // rebuild metadata of the verified rows (j <= Kp) and MASK rows (j > Kp)
   for (int j = tid; j < Kp + p.K; j += kThreads) {
     const int k = vb + j;
@@ -305,6 +294,26 @@ __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedStat
     if (p.sample_idx) {
       if (k == s) p.sample_idx[(long long)b * p.K] = t;
       if (j > Kp) p.sample_idx[(long long)b * p.K + (j - Kp)] = t;
+    }
+  }
+  if (tid == 0) {
+    const bool mine = (old & kXferCount) == (unsigned long long)nr;
+    if (mine) atomicExch(p.xfer + b, 0ull);  // both sides are done: clear for the next call
+    sh.xwrite = mine ? 1 : 0;
+  }
+  S::sync();
+  if (sh.xwrite) {  // every default write of this row happened before the tiles' counts
+    uint4* dst = p.X + (long long)(oo + s) * 2 * p.nvh;
+    const bool ok = bonus >= 0 && bonus < p.V;
+    const uint4* src = p.emb + (long long)bonus * p.nvh;
+    for (int v0 = 0; v0 < p.nvh; v0 += 2 * kThreads) {
+      const int v1 = v0 + tid, v2 = v0 + kThreads + tid;
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+      const uint4 x1 = ok && v1 < p.nvh ? __ldg(src + v1) : z;
+      const uint4 x2 = ok && v2 < p.nvh ? __ldg(src + v2) : z;
+      __threadfence();  // acquire side of the hand-off, before the stores
+      if (v1 < p.nvh) dst[v1] = x1;
+      if (v2 < p.nvh) dst[v2] = x2;
     }
   }
 }
