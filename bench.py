@@ -365,7 +365,9 @@ def run_ours(args):
     peak, peak_kind = measured_peak()
     achieved = bytes_["total"] / (mean_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                "frac": achieved / peak, "traffic": profiled_traffic(args.workload),
+                "frac": achieved / peak,
+                "traffic": profiled_traffic(args.workload,
+                                            "pe_step_early_exit" if args.early_exit else "pe_step"),
                 "peak_source": peak_kind, "algorithmic_bytes_per_launch": bytes_["total"],
                 "kernel": "pe::step_kernel<%s, early_exit=%s>" % (
                     "bf16" if spec.dtype == torch.bfloat16 else "f32",
