@@ -134,11 +134,22 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C / CUDA source without comments, trailing blanks and empty lines:
+    what the compiler sees, so that a comment edit keeps a profile current.
+    (String literals holding comment markers are not special-cased; the
+    kernel sources have none.)"""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_source_hash(sources=KERNEL_SOURCES) -> str:
+    """Hash of the kernel sources' code (comments ignored)."""
     h = hashlib.sha256()
     for rel in sources:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -16,19 +16,25 @@
 // Design (one launch, no grid-wide barrier, no spin-wait):
 //  * A persistent grid pulls work units from a counter in the workspace.
 //    Units [0, n_arg) are argmax chunks (row r, chunk c) of the logits, in
-//    row order; units [n_arg, n_units) copy tiles of X rows.
+//    row order; units [n_arg, n_units) copy tiles of X rows, first those of
+//    the verified rows, then those of the prompt and MASK rows (unit_at
+//    gives the order in which they are handed out).
 //  * Argmax chunk: 256 threads stream 32 KiB batches with 16-byte loads
 //    (eight per thread in flight), keep the thread's running maximum and the
 //    column where it first appears, reduce (value, column) keys with warp
 //    shuffles, and merge into the row's key with one 64-bit atomicMax.
 //  * The CTA whose chunk completes a request (per-request counter) runs
-//    that request's epilogue: accepted length, bonus token, the rebuild
-//    metadata of its verified and MASK slots, and the embedding half of the
-//    rows whose token depends on verification.
-//  * Copy tiles write everything of X that verification cannot change: the
-//    hidden half of every row, the MASK rows' emb(mask) (+) h_shared, and
-//    whole prompt rows (prefill) with their metadata.  The two kinds of
-//    writers touch disjoint bytes, so no ordering between them is needed.
+//    that request's epilogue, the verdict: accepted length, bonus token and
+//    the rebuild metadata of its verified and MASK slots.  It copies no
+//    embedding rows.
+//  * Copy tiles write all of X: the hidden half of every row, MASK rows
+//    whole (emb(mask) (+) h_shared), prompt rows whole (prefill) with their
+//    metadata, and the embedding half of every verified slot with the token
+//    it has unless it is the bonus slot.  The bonus row alone depends on the
+//    verdict: whichever of the verdict and the request's last verified-row
+//    tile comes second (one atomic each on the request's hand-off word)
+//    writes E[bonus] over the tile's default.  Every other byte of X has one
+//    writer.
 #include "pe_internal.cuh"
 #include "pe_tma.cuh"
 #include "pe_workspace.cuh"
@@ -197,9 +203,10 @@ struct Elem<PE_F32> {
 // Runs in the CTA that finished the last argmax chunk of request b.  Its
 // global traffic is two dependent round trips: (1) the row keys (exchanged
 // with 0, leaving the workspace clean), the drafts and the positions of the
-// verified rows, all at once; (2) after the verdict, the embedding rows of
-// the verified slots with their final tokens and the block-table entries of
-// the kept slots.
+// verified rows, all at once; (2) after the verdict, the hand-off atomic and
+// the block-table entries of the kept slots with the metadata stores; then,
+// only when the request's verified-row tiles are already done, the bonus
+// row's embedding half.
 // EARLY: the accepted length `a_known` is already settled (early-exit step);
 // rows 0..a_known are read from the completed-row results and later rows,
 // which may never have been read, report -1.
