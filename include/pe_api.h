@@ -74,6 +74,15 @@ typedef enum pe_dtype { PE_F32 = 0, PE_BF16 = 1 } pe_dtype;
 #define PE_ERR_ROW_RANGE 64u  /* readout row index outside [0,rows): -1     */
 #define PE_ERR_TIMEOUT 32u    /* a bounded pipeline wait gave up (outputs
                                  incomplete; never expected)               */
+/* Raised only by the checked build (libpe_checked.so: the same entry points
+ * compiled with PE_CHECKED, for debugging; slower).  Neither traps. */
+#define PE_ERR_NAN 128u       /* a logits row read by the greedy argmax
+                                 (pe_step, pe_step_early_exit,
+                                 pe_verify_greedy, pe_draft_readout) holds a
+                                 NaN; the outputs are then undefined        */
+#define PE_ERR_INTERNAL 256u  /* an internal index invariant of the fused
+                                 step failed; the access was skipped (never
+                                 expected: a library bug)                  */
 
 /* Limits checked on the host. */
 #define PE_MAX_KP 255 /* previous draft depth K'  */

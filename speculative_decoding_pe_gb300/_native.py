@@ -17,6 +17,9 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libpe.so")
+# the same ABI compiled with PE_CHECKED (NaN logits and internal invariants
+# raise ERR_NAN / ERR_INTERNAL; slower, for debugging)
+CHECKED_LIB_PATH = os.path.join(_HERE, "_build", "libpe_checked.so")
 
 PE_F32, PE_BF16 = 0, 1
 ERR_TOKEN_RANGE = 1
@@ -26,6 +29,8 @@ ERR_OFFSETS = 8
 ERR_MAP_RANGE = 16
 ERR_TIMEOUT = 32
 ERR_ROW_RANGE = 64
+ERR_NAN = 128
+ERR_INTERNAL = 256
 MAX_KP, MAX_K = 255, 256
 
 # every function the C header declares
@@ -81,41 +86,56 @@ def load():
     """Load libpe.so; raise if it has not been built."""
     global _lib
     with _lock:
-        if _lib is not None:
-            return _lib
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError(
-                "libpe.so is not built (%s); run speculative_decoding_pe_gb300.build."
-                "build() first -- there is no fallback path" % LIB_PATH)
-        lib = ctypes.CDLL(LIB_PATH)
-        lib.pe_workspace_bytes.argtypes = [i32, i32]
-        lib.pe_workspace_bytes.restype = ctypes.c_size_t
-        lib.pe_verify_greedy.argtypes = [P, ctypes.c_int, i64, i32, i32, i32, P, P, P,
-                                         P, P, P, P]
-        lib.pe_draft_readout.argtypes = [P, ctypes.c_int, i64, i32, i32, P, i32, P, P, P, P]
-        lib.pe_draft_readout.restype = ctypes.c_int
-        lib.pe_workspace_bytes_sampled.argtypes = [i32, i32]
-        lib.pe_workspace_bytes_sampled.restype = ctypes.c_size_t
-        lib.pe_verify_sampled.argtypes = [P, P, ctypes.c_int, i64, i64, i32, i32, i32, P, P,
-                                          ctypes.c_float, ctypes.c_uint64, P, P, P, P, P]
-        lib.pe_verify_sampled.restype = ctypes.c_int
-        lib.pe_build_draft_batch.argtypes = ([i32, i32, i32, i32, i32, P, P, P, P, P, P,
-                                              i32, i32] + [P] * 10)
-        lib.pe_assemble_draft_inputs.argtypes = [ctypes.c_int, i32, i32, i32, i32] + [P] * 9
-        lib.pe_step.argtypes = [ctypes.POINTER(StepArgs), P]
-        lib.pe_step_early_exit.argtypes = [ctypes.POINTER(StepArgs), P]
-        lib.pe_step_early_exit.restype = ctypes.c_int
-        lib.pe_step_noalloc.argtypes = [ctypes.POINTER(StepArgs), P]
-        lib.pe_step_noalloc.restype = ctypes.c_int
-        lib.pe_get_tuning.argtypes = [ctypes.POINTER(Tuning)]
-        lib.pe_set_tuning.argtypes = [ctypes.POINTER(Tuning)]
-        lib.pe_status_str.argtypes = [ctypes.c_int]
-        lib.pe_status_str.restype = ctypes.c_char_p
-        for f in ("pe_verify_greedy", "pe_build_draft_batch", "pe_assemble_draft_inputs",
-                  "pe_step", "pe_get_tuning", "pe_set_tuning"):
-            getattr(lib, f).restype = ctypes.c_int
-        _lib = lib
-        return lib
+        if _lib is None:
+            _lib = _open(LIB_PATH)
+        return _lib
+
+
+_checked = None
+
+
+def load_checked():
+    """Load libpe_checked.so (same entry points, PE_CHECKED); raise if absent."""
+    global _checked
+    with _lock:
+        if _checked is None:
+            _checked = _open(CHECKED_LIB_PATH)
+        return _checked
+
+
+def _open(path: str):
+    if not os.path.exists(path):
+        raise RuntimeError(
+            "%s is not built; run speculative_decoding_pe_gb300.build.build() first -- "
+            "there is no fallback path" % path)
+    lib = ctypes.CDLL(path)
+    lib.pe_workspace_bytes.argtypes = [i32, i32]
+    lib.pe_workspace_bytes.restype = ctypes.c_size_t
+    lib.pe_verify_greedy.argtypes = [P, ctypes.c_int, i64, i32, i32, i32, P, P, P,
+                                     P, P, P, P]
+    lib.pe_draft_readout.argtypes = [P, ctypes.c_int, i64, i32, i32, P, i32, P, P, P, P]
+    lib.pe_draft_readout.restype = ctypes.c_int
+    lib.pe_workspace_bytes_sampled.argtypes = [i32, i32]
+    lib.pe_workspace_bytes_sampled.restype = ctypes.c_size_t
+    lib.pe_verify_sampled.argtypes = [P, P, ctypes.c_int, i64, i64, i32, i32, i32, P, P,
+                                      ctypes.c_float, ctypes.c_uint64, P, P, P, P, P]
+    lib.pe_verify_sampled.restype = ctypes.c_int
+    lib.pe_build_draft_batch.argtypes = ([i32, i32, i32, i32, i32, P, P, P, P, P, P,
+                                          i32, i32] + [P] * 10)
+    lib.pe_assemble_draft_inputs.argtypes = [ctypes.c_int, i32, i32, i32, i32] + [P] * 9
+    lib.pe_step.argtypes = [ctypes.POINTER(StepArgs), P]
+    lib.pe_step_early_exit.argtypes = [ctypes.POINTER(StepArgs), P]
+    lib.pe_step_early_exit.restype = ctypes.c_int
+    lib.pe_step_noalloc.argtypes = [ctypes.POINTER(StepArgs), P]
+    lib.pe_step_noalloc.restype = ctypes.c_int
+    lib.pe_get_tuning.argtypes = [ctypes.POINTER(Tuning)]
+    lib.pe_set_tuning.argtypes = [ctypes.POINTER(Tuning)]
+    lib.pe_status_str.argtypes = [ctypes.c_int]
+    lib.pe_status_str.restype = ctypes.c_char_p
+    for f in ("pe_verify_greedy", "pe_build_draft_batch", "pe_assemble_draft_inputs",
+              "pe_step", "pe_get_tuning", "pe_set_tuning"):
+        getattr(lib, f).restype = ctypes.c_int
+    return lib
 
 
 # ------------------------------------------------------------------ helpers

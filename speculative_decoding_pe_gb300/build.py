@@ -17,6 +17,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(OUT_DIR, "libpe.so")
+# The same entry points compiled with PE_CHECKED: NaN logits and internal
+# index invariants raise error bits (slower; for debugging).
+CHECKED_LIB_PATH = os.path.join(OUT_DIR, "libpe_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
@@ -39,29 +42,29 @@ def _inputs() -> list[str]:
             glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)])
 
 
-def is_stale() -> bool:
-    if not os.path.exists(LIB_PATH):
+def is_stale(lib: str = LIB_PATH) -> bool:
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB_PATH)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(p) > t for p in _inputs())
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    """Compile and link libpe.so when it is missing or older than a source."""
-    if not force and not is_stale():
-        return LIB_PATH
-    obj_dir = os.path.join(OUT_DIR, "obj")
+def _compile(lib: str, obj_dir: str, defines: list[str], verbose_ptxas: bool):
+    """Start one nvcc process per source; returns (objects, processes)."""
     os.makedirs(obj_dir, exist_ok=True)
     nvcc = _nvcc()
     extra = ["-Xptxas", "-v"] if verbose_ptxas else []
-    procs = []
-    objs = []
+    procs, objs = [], []
     for src in sources():
         obj = os.path.join(obj_dir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
-        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj]
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, *defines, *extra, "-c", src, "-o", obj]
         procs.append((src, subprocess.Popen(cmd, stdout=subprocess.PIPE,
                                             stderr=subprocess.STDOUT, text=True)))
+    return objs, procs
+
+
+def _finish(lib: str, objs, procs, verbose_ptxas: bool):
     failed = []
     for src, p in procs:
         out, _ = p.communicate()
@@ -71,9 +74,21 @@ def build(force: bool = False, verbose_ptxas: bool = False) -> str:
             failed.append(src)
     if failed:
         raise RuntimeError("nvcc failed on: %s" % ", ".join(failed))
-    tmp = LIB_PATH + ".tmp%d" % os.getpid()
-    subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], check=True)
-    os.replace(tmp, LIB_PATH)
+    tmp = lib + ".tmp%d" % os.getpid()
+    subprocess.run([_nvcc(), *ARCH, "-shared", "-o", tmp, *objs], check=True)
+    os.replace(tmp, lib)
+
+
+def build(force: bool = False, verbose_ptxas: bool = False, checked: bool = True) -> str:
+    """Compile and link libpe.so (and libpe_checked.so) when missing or older
+    than a source; the two compile in parallel."""
+    jobs = [(LIB_PATH, os.path.join(OUT_DIR, "obj"), [])]
+    if checked:
+        jobs.append((CHECKED_LIB_PATH, os.path.join(OUT_DIR, "obj_checked"), ["-DPE_CHECKED"]))
+    started = [(lib, *_compile(lib, d, defs, verbose_ptxas)) for lib, d, defs in jobs
+               if force or is_stale(lib)]
+    for lib, objs, procs in started:
+        _finish(lib, objs, procs, verbose_ptxas)
     return LIB_PATH
 
 

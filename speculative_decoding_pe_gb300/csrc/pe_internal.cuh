@@ -57,6 +57,31 @@ __device__ __forceinline__ unsigned long long warp_max_key(unsigned long long k)
   return k;
 }
 
+// ------------------------------------------------------------ checked build
+// PE_CHECKED (libpe_checked.so): an internal index invariant that fails
+// raises PE_ERR_INTERNAL and the access it guards is skipped; in the
+// regular build the condition is not evaluated.
+#ifdef PE_CHECKED
+#define PE_INVARIANT(err, cond) ((cond) || (atomicOr((err), PE_ERR_INTERNAL), false))
+#else
+#define PE_INVARIANT(err, cond) true
+#endif
+
+// NaN among the elements of a 16-byte vector (exponent all ones, mantissa
+// not zero), by the bit patterns of the formats.
+__device__ __forceinline__ bool bf16x8_has_nan(uint4 q) {
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  bool n = false;
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    n |= (w[i] & 0x7fffu) > 0x7f80u || ((w[i] >> 16) & 0x7fffu) > 0x7f80u;
+  return n;
+}
+__device__ __forceinline__ bool f32x4_has_nan(uint4 q) {
+  return (q.x & 0x7fffffffu) > 0x7f800000u || (q.y & 0x7fffffffu) > 0x7f800000u ||
+         (q.z & 0x7fffffffu) > 0x7f800000u || (q.w & 0x7fffffffu) > 0x7f800000u;
+}
+
 // ------------------------------------------------------------------ KV slots
 // Paged-KV slot of a kept position; -1 (and an error bit) outside the table.
 __device__ __forceinline__ long long kv_slot(const int32_t* block_table,

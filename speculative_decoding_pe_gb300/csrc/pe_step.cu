@@ -152,6 +152,7 @@ struct Elem;
 template <>
 struct Elem<PE_BF16> {
   static constexpr int kPerVec = 8;
+  __device__ static __forceinline__ bool has_nan(uint4 q) { return bf16x8_has_nan(q); }
   __device__ static __forceinline__ uint4 neg_inf() {
     return make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
   }
@@ -180,6 +181,7 @@ struct Elem<PE_BF16> {
 template <>
 struct Elem<PE_F32> {
   static constexpr int kPerVec = 4;
+  __device__ static __forceinline__ bool has_nan(uint4 q) { return f32x4_has_nan(q); }
   __device__ static __forceinline__ uint4 neg_inf() {
     return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
   }
@@ -281,6 +283,8 @@ __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedStat
   for (int j = tid; j < Kp + p.K; j += kThreads) {
     const int k = vb + j;
     const int t = oo + k;
+    if (!PE_INVARIANT(p.err, t >= 0 && t < p.T && (j > Kp || (io + k >= 0 && io + k < p.R))))
+      continue;
     int tok, pos, rej = 0, msk = 0;
     if (j <= Kp) {
       tok = slot_token(j);
@@ -309,7 +313,8 @@ __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedStat
     sh.xwrite = mine ? 1 : 0;
   }
   S::sync();
-  if (sh.xwrite) {  // every default write of this row happened before the tiles' counts
+  if (sh.xwrite && PE_INVARIANT(p.err, oo + s >= 0 && oo + s < p.T)) {
+    // every default write of this row happened before the tiles' counts
     uint4* dst = p.X + (long long)(oo + s) * 2 * p.nvh;
     const bool ok = bonus >= 0 && bonus < p.V;
     const uint4* src = p.emb + (long long)bonus * p.nvh;
@@ -335,12 +340,17 @@ __device__ __forceinline__ void finish_argmax_unit(const StepParams& p, SharedSt
 // [v_lo, v_hi) of one logits row.  Elements are visited in increasing column
 // order (batch, then vector i, then element), so a strict '>' keeps the
 // first occurrence.
+// Checked build: a NaN among the elements read raises PE_ERR_NAN in *err.
 template <int DT>
-__device__ __forceinline__ unsigned long long thread_key(const uint4* row, int v_lo, int v_hi) {
+__device__ __forceinline__ unsigned long long thread_key(const uint4* row, int v_lo, int v_hi,
+                                                         uint32_t* err) {
   using E = Elem<DT>;
   const int tid = threadIdx.x;
   float m = 0.f;
   int col = -1;
+#ifdef PE_CHECKED
+  bool nan = false;
+#endif
   for (int base = v_lo; base < v_hi; base += kBatchVecs) {
     if (base + tid >= v_hi) break;  // this thread has no vector here or later
     uint4 x[kVecPerThread];
@@ -349,6 +359,10 @@ __device__ __forceinline__ unsigned long long thread_key(const uint4* row, int v
       const int v = base + i * kThreads + tid;
       x[i] = v < v_hi ? __ldcs(row + v) : E::neg_inf();
     }
+#ifdef PE_CHECKED
+#pragma unroll
+    for (int i = 0; i < kVecPerThread; ++i) nan |= E::has_nan(x[i]);
+#endif
     float vm[kVecPerThread];
 #pragma unroll
     for (int i = 0; i < kVecPerThread; ++i) vm[i] = E::vmax(x[i]);
@@ -369,6 +383,11 @@ __device__ __forceinline__ unsigned long long thread_key(const uint4* row, int v
       col = (base + vi * kThreads + tid) * E::kPerVec + E::first_equal(q, gm);
     }
   }
+#ifdef PE_CHECKED
+  if (nan) atomicOr(err, PE_ERR_NAN);
+#else
+  (void)err;
+#endif
   return col >= 0 ? make_key(m, (uint32_t)col) : 0ull;
 }
 
@@ -382,7 +401,7 @@ __device__ __forceinline__ void argmax_unit(const StepParams& p, SharedState& sh
   const int v_hi = rowp ? min(v_lo + p.chunk_vecs, p.nvec) : v_lo;  // bad index: nothing
   if (!rowp && c == 0 && tid == 0) atomicOr(p.err, PE_ERR_ROW_RANGE);
   const unsigned long long key =
-      thread_key<DT>(reinterpret_cast<const uint4*>(rowp), v_lo, v_hi);
+      thread_key<DT>(reinterpret_cast<const uint4*>(rowp), v_lo, v_hi, p.err);
   finish_argmax_unit<SyncAll, DT>(p, sh, r, c, rowp, key);
 }
 
@@ -400,13 +419,22 @@ __device__ __forceinline__ void finish_argmax_unit(const StepParams& p, SharedSt
     const int c0 = p.nvec * E::kPerVec;
     float tm = E::scalar(rowp, c0);
     int tc = c0;
+#ifdef PE_CHECKED
+    bool nan = tm != tm;
+#endif
     for (int e = 1; e < p.tail; ++e) {
       const float x = E::scalar(rowp, c0 + e);
+#ifdef PE_CHECKED
+      nan |= x != x;
+#endif
       if (x > tm) {
         tm = x;
         tc = c0 + e;
       }
     }
+#ifdef PE_CHECKED
+    if (nan) atomicOr(p.err, PE_ERR_NAN);
+#endif
     const unsigned long long tk = make_key(tm, (uint32_t)tc);
     key = tk > key ? tk : key;
   }
@@ -467,18 +495,28 @@ __device__ __forceinline__ void argmax_unit_early(const StepParams& p, SharedSta
   const char* rowp = logits_row(p, r);
   const int v_lo = c * p.chunk_vecs;
   const int v_hi = min(v_lo + p.chunk_vecs, p.nvec);
-  unsigned long long key = thread_key<DT>(reinterpret_cast<const uint4*>(rowp), v_lo, v_hi);
+  unsigned long long key =
+      thread_key<DT>(reinterpret_cast<const uint4*>(rowp), v_lo, v_hi, p.err);
   if (p.tail && c == p.C - 1 && tid == 0) {  // leftover elements past the last vector
     const int c0 = p.nvec * E::kPerVec;
     float tm = E::scalar(rowp, c0);
     int tc = c0;
+#ifdef PE_CHECKED
+    bool nan = tm != tm;
+#endif
     for (int e = 1; e < p.tail; ++e) {
       const float x = E::scalar(rowp, c0 + e);
+#ifdef PE_CHECKED
+      nan |= x != x;
+#endif
       if (x > tm) {
         tm = x;
         tc = c0 + e;
       }
     }
+#ifdef PE_CHECKED
+    if (nan) atomicOr(p.err, PE_ERR_NAN);
+#endif
     const unsigned long long tk = make_key(tm, (uint32_t)tc);
     key = tk > key ? tk : key;
   }
@@ -583,7 +621,12 @@ __device__ __forceinline__ void copy_unit(const StepParams& p, SharedState& sh, 
     int me;
     const uint4* se = nullptr;
     const uint4* sh_src;
-    if (k < vb) {  // prompt row: shifted token, own hidden row
+    sh.vreq[tid] = -1;
+    if (!PE_INVARIANT(p.err, t >= 0 && t < p.T && b >= 0 && b < p.B && k >= 0 && k < n + p.K - 1)) {
+      me = kSkip;  // (checked build only) leave the row alone
+      sh_src = nullptr;
+      xr = nullptr;
+    } else if (k < vb) {  // prompt row: shifted token, own hidden row
       const int tok = __ldg(p.in_tokens + io + k + 1);
       const int pos = __ldg(p.in_positions + io + k);
       p.out_tokens[t] = tok;
@@ -625,9 +668,9 @@ __device__ __forceinline__ void copy_unit(const StepParams& p, SharedState& sh, 
     sh.mode[2 * tid] = me;
     sh.src[2 * tid] = se;
     sh.dst[2 * tid] = xr;
-    sh.mode[2 * tid + 1] = kCopy;
+    sh.mode[2 * tid + 1] = xr ? kCopy : kSkip;
     sh.src[2 * tid + 1] = sh_src;
-    sh.dst[2 * tid + 1] = xr + p.nvh;
+    sh.dst[2 * tid + 1] = xr ? xr + p.nvh : nullptr;
   }
   if (tid == 0) sh.nbonus = 0;
   S::sync();
@@ -668,7 +711,7 @@ __device__ __forceinline__ void copy_unit(const StepParams& p, SharedState& sh, 
   // verdict comes later, the verdict writes it.
   __threadfence();
   S::sync();
-  if (tid < nrows) {
+  if (tid < nrows && sh.vreq[tid] >= 0) {
     const int b = sh.vreq[tid];
     const unsigned long long old = atomicAdd(p.xfer + b, 1ull);
     if ((old & kXferCount) + 1 == (unsigned long long)(p.Kp + 1) && (old & kXferVerdict)) {
@@ -924,6 +967,9 @@ __device__ __forceinline__ void consume(const StepParams& p, SharedState& sh, co
       if (lane == 0) mbar_arrive(&empty[stage]);  // this warp is done with the stage
 #pragma unroll
       for (int k = 0; k < kStageVecs / kThreads; ++k) {
+#ifdef PE_CHECKED
+        if (k * kThreads + tid < in.n && E::has_nan(x[k])) atomicOr(p.err, PE_ERR_NAN);
+#endif
         const float vm = E::vmax(x[k]);
         const bool valid = k * kThreads + tid < in.n;
         if (valid && (qv < 0 || vm > m)) {  // pieces and k run in increasing column order

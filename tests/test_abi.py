@@ -38,6 +38,13 @@ def test_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_checked_build_exports_the_same_symbols(lib):
+    checked = _native.load_checked()
+    for name in declared_functions():
+        assert hasattr(checked, name), name
+    assert checked.pe_workspace_bytes(2048, 256) == lib.pe_workspace_bytes(2048, 256)
+
+
 def test_status_strings(lib):
     for code in (0, -1, -2, -3, -4):
         s = lib.pe_status_str(code).decode()
