@@ -555,6 +555,103 @@ def run_sampled(args):
     return 0
 
 
+READOUT_METRIC = "greedy drafter readout rows/s"
+READOUT_SHAPE = {"B": 256, "K": 7, "V": 151936}  # the large-batch decode shape
+
+
+def run_readout(args):
+    """Time pe_draft_readout (one launch) on the drafter's logits for the K
+    sampled rows of each of B requests: argmax of B*K rows of V columns,
+    bf16, N(0, 2), the drafter computing only the sampled rows."""
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(world, "nccl")
+    from speculative_decoding_pe_gb300 import _native
+    _native.load()
+    B, K, V = READOUT_SHAPE["B"], READOUT_SHAPE["K"], READOUT_SHAPE["V"]
+    n = B * K
+    g = torch.Generator(device=device)
+    g.manual_seed(7300 + rank)
+    logits = (torch.randn(n, V, generator=g, device=device) * 2.0).to(torch.bfloat16)
+    out = torch.empty(n, dtype=torch.int32, device=device)
+    ws = _native.new_workspace(n, n, device)
+    err = _native.new_error_word(device)
+    l2 = torch.cuda.get_device_properties(device).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        _native.draft_readout(logits, out, ws, err, None, stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize(device)
+    if int(err.item()) != 0 or int(ws.count_nonzero()) != 0:
+        raise SystemExit("device error word or workspace not zero after warm-up")
+    sampler = ClockSampler(local)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize(device)
+    t_wall0 = time.time()
+    torch.cuda.nvtx.range_push("timed")
+    for e0, e1 in ev:
+        flush.zero_()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize(device)
+    barrier(world)
+    t_wall1 = time.time()
+    clocks = sampler.stop(t_wall0, t_wall1)
+    step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
+    mean_ms = sum(step_ms) / len(step_ms)
+    value, mean_ms_max, _ = aggregate(float(n), mean_ms, world, device)
+    total = n * V * 2 + 4 * n  # logits read once, tokens written
+    peak, peak_kind = measured_peak()
+    achieved = total / (mean_ms / 1e3) / 1e9
+
+    cpu = None
+    if rank == 0 and world == 1 and args.cpu_baseline:
+        import oracle  # CPU baseline leg only
+        rows = 64
+        host = logits[:rows].cpu()
+        times = []
+        t_end = time.time() + args.cpu_budget
+        while len(times) < 3 or time.time() < t_end:
+            t0 = time.perf_counter()
+            oracle.draft_readout(host)
+            times.append(time.perf_counter() - t0)
+        t = statistics.median(times)
+        cpu = {"value": rows / t, "unit": "rows/s", "cores": 1, "kind": "oracle",
+               "sample": "first %d of %d rows, %d runs, median %.1f ms, single-threaded C "
+                         "oracle on %s" % (rows, n, len(times), t * 1e3, cpu_model())}
+    if rank == 0:
+        print(json.dumps({
+            "metric": READOUT_METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms_max,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": "greedy drafter readout B=%d K=%d V=%d bf16" % (B, K, V),
+                       "l2": "flushed between steps (2x L2 written)",
+                       "median_us": statistics.median(step_ms) * 1e3,
+                       "min_us": min(step_ms) * 1e3,
+                       "tuning": _native.get_tuning()},
+            "us_per_step": mean_ms_max * 1e3,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "traffic": None,
+                         "peak_source": peak_kind, "algorithmic_bytes_per_launch": total,
+                         "kernel": "pe::step_kernel<bf16> (readout: argmax units only)"},
+            "cpu_baseline": cpu, "gpu_launches": args.steps, "clocks": clocks}))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
 def measure_e2e(w, out, ws, err, packed, stream, device, args):
     """The same step through the public API with inputs copied in from pinned
     host memory and the per-request results copied back, every step."""
@@ -659,6 +756,8 @@ def main(argv=None):
     ap.add_argument("--early-exit", action="store_true",
                     help="time pe_step_early_exit (rows after each request's first "
                          "mismatch are not read)")
+    ap.add_argument("--readout", action="store_true",
+                    help="time the greedy drafter readout (B=256 x K=7 rows, V=151936)")
     ap.add_argument("--sampled", action="store_true",
                     help="time rejection-sampling verification (pe_verify_sampled) "
                          "instead of the fused greedy step")
@@ -674,6 +773,8 @@ def main(argv=None):
         return run_reference(args)
     if args.sampled:
         return run_sampled(args)
+    if args.readout:
+        return run_readout(args)
     return run_ours(args)
 
 
