@@ -47,7 +47,8 @@ struct SampledParams {
   int32_t* bonus_token;
   uint32_t* err;
   // workspace
-  uint32_t* sched;            // [4] stats: unit counter, CTAs done; residual: same
+  uint32_t* sched;            // [8] stats: unit counter, CTAs done; residual: same;
+                              // [4]: requests listed for a residual draw
   float2* partial;            // [Rt+Rd][kMaxChunksSampled] (max, sum) per chunk
   float* lse;                 // [Rt+Rd] log2 of the row's normaliser (log2 domain)
   float* prob;                // [Rt+Rd] p(x) or q(x) of the row's draft token
@@ -57,6 +58,7 @@ struct SampledParams {
   int32_t* acc;               // [B] accepted length, for the residual pass
   unsigned long long* gkey;   // [B] Gumbel draw from the bonus row
   unsigned long long* rkey;   // [B] Gumbel draw from the residual
+  int32_t* rlist;             // [sched[4]] requests with a rejection, in decision order
 };
 
 // ------------------------------------------------------------ Philox4x32-10
@@ -360,7 +362,10 @@ __device__ __forceinline__ void decide(const SampledParams& p, int b) {
     }
   }
   p.accepted_len[b] = a;
-  p.acc[b] = a;
+  if (a < p.Kp) {  // a rejection: list the request for the residual pass
+    p.acc[b] = a;  // (the residual draw clears it)
+    p.rlist[atomicAdd(p.sched + 4, 1u)] = b;
+  }
   const unsigned long long gk = atomicExch(p.gkey + b, 0ull);
   if (a == p.Kp) p.bonus_token[b] = (int)key_col(gk);  // else the residual pass draws
   for (int j = 0; j <= p.Kp; ++j) {
@@ -490,7 +495,8 @@ __global__ void __launch_bounds__(kThreads, kStatsCtasPerSm) sampled_stats_kerne
   }
 }
 
-// Residual draw of request b, chunk c (warp unit u = b * C2 + c): Gumbel-max
+// Residual draw of request b, chunk c (u = b * C2 + c; only listed requests,
+// which all have a rejection, get units): Gumbel-max
 // over log2 max(0, p - q) with p = 2^(y_t - L_t), q = 2^(y_d - L_d).  The
 // warp that completes the request publishes the draw; should the residual be
 // empty (p == q everywhere, possible only for identical rows) that warp
@@ -595,24 +601,32 @@ __device__ __forceinline__ void residual_unit(const SampledParams& p, int u, int
   }
 }
 
+// Persistent warps over the residual units of the listed requests
+// (sched[2]: unit counter, sched[3]: warps done); the list is complete, the
+// stats pass having finished.  The last warp to leave clears the list and
+// the counter words.
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 4) sampled_residual_kernel(const SampledParams p) {
   const int lane = threadIdx.x & 31;
-  const int n_units = p.B * p.C2;
+  const int n_units = (int)__ldcg(p.sched + 4) * p.C2;
   int u = 0;
   if (lane == 0) u = (int)atomicAdd(p.sched + 2, 1u);
   u = __shfl_sync(0xffffffffu, u, 0);
   while (u < n_units) {
     int next = 0;
     if (lane == 0) next = (int)atomicAdd(p.sched + 2, 1u);
-    residual_unit<DT>(p, u, lane);
+    const int k = u / p.C2;
+    residual_unit<DT>(p, __ldcg(p.rlist + k) * p.C2 + (u - k * p.C2), lane);
     u = __shfl_sync(0xffffffffu, next, 0);
   }
   if (lane == 0) {
     __threadfence();
-    if (atomicAdd(p.sched + 3, 1u) == gridDim.x * kWarps - 1) {
+    if (atomicAdd(p.sched + 3, 1u) == gridDim.x * kWarps - 1) {  // every other warp has left
+      const unsigned listed = p.sched[4];
+      for (unsigned k = 0; k < listed; ++k) p.rlist[k] = 0;
       atomicExch(p.sched + 2, 0u);
       atomicExch(p.sched + 3, 0u);
+      atomicExch(p.sched + 4, 0u);
     }
   }
 }
@@ -624,10 +638,10 @@ namespace {
 
 struct SampledLayout {
   size_t partial_off, lse_off, prob_off, rcount_off, qcount_off, dcount_off, acc_off, gkey_off,
-      rkey_off, bytes;
+      rkey_off, rlist_off, bytes;
   SampledLayout(long long B, long long Kp) {
     const long long rows = B * (Kp + 1) + B * Kp;
-    size_t o = 16;  // four scheduler words
+    size_t o = 32;  // eight scheduler words
     auto take = [&](size_t n, size_t align) {
       o = (o + align - 1) / align * align;
       const size_t at = o;
@@ -643,6 +657,7 @@ struct SampledLayout {
     acc_off = take(4 * B, 16);
     gkey_off = take(8 * B, 16);
     rkey_off = take(8 * B, 16);
+    rlist_off = take(4 * B, 16);
     bytes = (o + 255) / 256 * 256;
   }
 };
@@ -731,6 +746,7 @@ int pe_verify_sampled(const void* target_logits, const void* draft_logits, int d
   p.acc = reinterpret_cast<int32_t*>(w + L.acc_off);
   p.gkey = reinterpret_cast<unsigned long long*>(w + L.gkey_off);
   p.rkey = reinterpret_cast<unsigned long long*>(w + L.rkey_off);
+  p.rlist = reinterpret_cast<int32_t*>(w + L.rlist_off);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   // persistent grids: 3 CTAs (24 warps) per SM, fewer for small problems
