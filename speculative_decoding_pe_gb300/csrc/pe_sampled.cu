@@ -47,7 +47,8 @@ struct SampledParams {
   int32_t* bonus_token;
   uint32_t* err;
   // workspace
-  uint32_t* sched;            // [8] stats: unit counter, CTAs done; residual: same;
+  uint32_t* sched;            // [8] [0] stats unit counter; [2], [3] residual unit
+                              // counter and warps done;
                               // [4]: requests listed for a residual draw
   float2* partial;            // [Rt+Rd][kMaxChunksSampled] (max, sum) per chunk
   float* lse;                 // [Rt+Rd] log2 of the row's normaliser (log2 domain)
@@ -468,9 +469,16 @@ __device__ __forceinline__ void stats_unit(const SampledParams& p, int u, int la
 }
 
 // Persistent warps over a dynamic unit counter (sched[0]); the next unit is
-// fetched before the current one is processed.  The last warp to leave
-// resets the counter words (sched[0], sched[1]).
+// fetched before the current one is processed.  Every warp takes exactly one
+// index past the last unit and then no other, so the warp that receives the
+// last such index (n_units + warps - 1) resets the counter.
 constexpr int kStatsCtasPerSm = 4;  // 32 warps per SM: 64 registers a thread
+
+__device__ __forceinline__ int stats_claim(const SampledParams& p, int n_units) {
+  const unsigned v = atomicAdd(p.sched, 1u);
+  if (v == (unsigned)n_units + gridDim.x * kWarps - 1u) atomicExch(p.sched, 0u);
+  return (int)v;
+}
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads, kStatsCtasPerSm) sampled_stats_kernel(
@@ -478,20 +486,13 @@ __global__ void __launch_bounds__(kThreads, kStatsCtasPerSm) sampled_stats_kerne
   const int lane = threadIdx.x & 31;
   const int n_units = (p.Rt + p.Rd) * p.C;
   int u = 0;
-  if (lane == 0) u = (int)atomicAdd(p.sched, 1u);
+  if (lane == 0) u = stats_claim(p, n_units);
   u = __shfl_sync(0xffffffffu, u, 0);
   while (u < n_units) {
     int next = 0;
-    if (lane == 0) next = (int)atomicAdd(p.sched, 1u);
+    if (lane == 0) next = stats_claim(p, n_units);
     stats_unit<DT>(p, u, lane);
     u = __shfl_sync(0xffffffffu, next, 0);
-  }
-  if (lane == 0) {
-    __threadfence();
-    if (atomicAdd(p.sched + 1, 1u) == gridDim.x * kWarps - 1) {
-      atomicExch(p.sched, 0u);
-      atomicExch(p.sched + 1, 0u);
-    }
   }
 }
 

@@ -279,6 +279,13 @@ __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedStat
   if (tid == 0)
     old = atomicOr(p.xfer + b, kXferVerdict | ((unsigned long long)a << 17) |
                                    ((unsigned long long)(uint32_t)bonus << 32));
+  // the bonus row's first 2*kThreads vectors, read now in case this verdict
+  // is the one to write it (the embedding table never changes)
+  const bool bok = bonus >= 0 && bonus < p.V;
+  const uint4* bsrc = p.emb + (long long)bonus * p.nvh;
+  const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+  const uint4 x1 = bok && tid < p.nvh ? __ldg(bsrc + tid) : zero;
+  const uint4 x2 = bok && kThreads + tid < p.nvh ? __ldg(bsrc + kThreads + tid) : zero;
   // rebuild metadata of the verified rows (j <= Kp) and MASK rows (j > Kp)
   for (int j = tid; j < Kp + p.K; j += kThreads) {
     const int k = vb + j;
@@ -316,17 +323,11 @@ __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedStat
   if (sh.xwrite && PE_INVARIANT(p.err, oo + s >= 0 && oo + s < p.T)) {
     // every default write of this row happened before the tiles' counts
     uint4* dst = p.X + (long long)(oo + s) * 2 * p.nvh;
-    const bool ok = bonus >= 0 && bonus < p.V;
-    const uint4* src = p.emb + (long long)bonus * p.nvh;
-    for (int v0 = 0; v0 < p.nvh; v0 += 2 * kThreads) {
-      const int v1 = v0 + tid, v2 = v0 + kThreads + tid;
-      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-      const uint4 x1 = ok && v1 < p.nvh ? __ldg(src + v1) : z;
-      const uint4 x2 = ok && v2 < p.nvh ? __ldg(src + v2) : z;
-      __threadfence();  // acquire side of the hand-off, before the stores
-      if (v1 < p.nvh) dst[v1] = x1;
-      if (v2 < p.nvh) dst[v2] = x2;
-    }
+    __threadfence();  // acquire side of the hand-off, before the stores
+    if (tid < p.nvh) dst[tid] = x1;
+    if (kThreads + tid < p.nvh) dst[kThreads + tid] = x2;
+    for (int v = 2 * kThreads + tid; v < p.nvh; v += kThreads)
+      dst[v] = bok ? __ldg(bsrc + v) : zero;
   }
 }
 
@@ -764,16 +765,17 @@ __global__ void __launch_bounds__(kThreads, 4) step_kernel(const StepParams p) {
     else
       copy_tile<SyncAll>(p, sh, u - p.n_arg_units);
     __syncthreads();
-    if (threadIdx.x == 0) sh.unit = (int)(gridDim.x + atomicAdd(p.sched, 1u));
+    if (threadIdx.x == 0) {
+      // The counter hands out n_units - gridDim.x units, then one index past
+      // the end to each CTA, after which that CTA never touches it again: the
+      // CTA that receives the last index (n_units - 1) is the last to finish
+      // and resets the counter for the next call.
+      const unsigned v = atomicAdd(p.sched, 1u);
+      if (v == (unsigned)p.n_units - 1u) atomicExch(p.sched, 0u);
+      sh.unit = (int)(gridDim.x + v);
+    }
     __syncthreads();
     q = sh.unit;
-  }
-  if (threadIdx.x == 0) {
-    __threadfence();
-    if (atomicAdd(p.sched + 1, 1u) == gridDim.x - 1) {  // every other CTA has left
-      atomicExch(p.sched, 0u);
-      atomicExch(p.sched + 1, 0u);
-    }
   }
 }
 
