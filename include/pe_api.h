@@ -72,8 +72,9 @@ typedef enum pe_dtype { PE_F32 = 0, PE_BF16 = 1 } pe_dtype;
 #define PE_ERR_OFFSETS 8u     /* in_offsets invalid: nothing is written     */
 #define PE_ERR_MAP_RANGE 16u  /* hidden_map entry outside [0,T): skipped    */
 #define PE_ERR_ROW_RANGE 64u  /* readout row index outside [0,rows): -1     */
-#define PE_ERR_TIMEOUT 32u    /* a bounded pipeline wait gave up (outputs
-                                 incomplete; never expected)               */
+#define PE_ERR_TIMEOUT 32u    /* a bounded wait gave up (the pipelined
+                                 step's ring, the sampled stats merge);
+                                 outputs incomplete; never expected        */
 /* Raised only by the checked build (libpe_checked.so: the same entry points
  * compiled with PE_CHECKED, for debugging; slower).  Neither traps. */
 #define PE_ERR_NAN 128u       /* a logits row read by the greedy argmax

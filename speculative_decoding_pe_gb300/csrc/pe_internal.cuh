@@ -31,6 +31,19 @@ __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
   return d;
 }
 
+// ------------------------------------------------------------------- ordering
+// Device-scope release/acquire fence.  Every hand-off between CTAs or warps
+// here is message passing: data stores, then a counter (or bit) update that
+// tells the last arrival to read them.  That needs release ordering at the
+// writer (fence, then the counter update, in the updating thread, after any
+// barrier that gathers the other threads' stores) and acquire ordering at
+// the reader (the update that reveals completion, then the fence, in that
+// same thread, before the barrier that releases the other threads' loads).
+// Sequential consistency (the fence __threadfence() gives) is not needed.
+__device__ __forceinline__ void fence_acq_rel() {
+  asm volatile("fence.acq_rel.gpu;" ::: "memory");
+}
+
 // Total order on non-NaN floats as unsigned integers, with -0.0 == +0.0.
 __device__ __forceinline__ uint32_t ordered_bits(float f) {
   uint32_t b = __float_as_uint(f);

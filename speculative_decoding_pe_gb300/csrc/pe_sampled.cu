@@ -50,7 +50,8 @@ struct SampledParams {
   uint32_t* sched;            // [8] [0] stats unit counter; [2], [3] residual unit
                               // counter and warps done;
                               // [4]: requests listed for a residual draw
-  float2* partial;            // [Rt+Rd][kMaxChunksSampled] (max, sum) per chunk
+  unsigned long long* partial;  // [Rt+Rd][kMaxChunksSampled] (max, sum) per chunk,
+                                // packed by pack_partial (0: not yet written)
   float* lse;                 // [Rt+Rd] log2 of the row's normaliser (log2 domain)
   float* prob;                // [Rt+Rd] p(x) or q(x) of the row's draft token
   uint32_t* rcount;           // [Rt+Rd] finished chunks per row
@@ -349,6 +350,31 @@ __device__ __forceinline__ void fold_chunk(const SampledParams& p, const char* r
   }
 }
 
+// A chunk's (max, sum) in one 64-bit word that is never zero, so that zero
+// (the workspace's resting state) marks a slot not yet written: the max is
+// never NaN (it starts finite and only takes larger values), and its bits
+// are stored XOR a quiet-NaN pattern.
+constexpr uint32_t kPartialMark = 0x7fc00000u;
+constexpr int kPollLimit = 1 << 20;  // loads of a slot before giving up
+
+__device__ __forceinline__ unsigned long long pack_partial(float2 t) {
+  return ((unsigned long long)(__float_as_uint(t.x) ^ kPartialMark) << 32) | __float_as_uint(t.y);
+}
+__device__ __forceinline__ float2 unpack_partial(unsigned long long w) {
+  return make_float2(__uint_as_float((uint32_t)(w >> 32) ^ kPartialMark),
+                     __uint_as_float((uint32_t)w));
+}
+// Strong (relaxed, device-scope) 64-bit store and load: single-copy atomic,
+// so a poller sees either zero or the whole word.
+__device__ __forceinline__ void st_relaxed(unsigned long long* a, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(a), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long* a) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
+  return v;
+}
+
 // Accepted length of request b from its rows' draft-token probabilities.
 // Leaves the workspace zeroed except the normalisers the residual draw of
 // this request reads (target and draft row a); that draw clears them.
@@ -419,19 +445,31 @@ __device__ __forceinline__ void stats_finish(const SampledParams& p, int vr, int
   }
   const float2 t = warp_combine(make_float2(m, s));
   const unsigned long long gk = draw ? warp_max_key(bt.key()) : 0ull;
+  // The partial goes out without a fence: the warp that completes the row
+  // polls each slot until it holds a value.  Only the bonus row's key (an
+  // atomicMax elsewhere) needs the release before the count.
   int last = 0;
   if (lane == 0) {
-    p.partial[vr * kMaxChunksSampled + c] = t;
-    if (draw) atomicMax(p.gkey + b, gk);
-    __threadfence();
+    st_relaxed(p.partial + vr * kMaxChunksSampled + c, pack_partial(t));
+    if (draw) {
+      atomicMax(p.gkey + b, gk);
+      fence_acq_rel();  // release
+    }
     last = atomicAdd(p.rcount + vr, 1u) == (unsigned)(p.C - 1);
+    if (last) fence_acq_rel();  // acquire: the bonus row's key
   }
   if (!__shfl_sync(0xffffffffu, last, 0)) return;
-  __threadfence();
+  __syncwarp();  // orders lane 0's acquire before the other lanes' accesses
   float2 acc = make_float2(-3.0e38f, 0.f);
   for (int cc = lane; cc < p.C; cc += 32) {
-    acc = combine(acc, __ldcg(p.partial + vr * kMaxChunksSampled + cc));
-    p.partial[vr * kMaxChunksSampled + cc] = make_float2(0.f, 0.f);
+    unsigned long long* slot = p.partial + vr * kMaxChunksSampled + cc;
+    unsigned long long w = ld_relaxed(slot);
+    for (int it = 0; w == 0ull && it < kPollLimit; ++it) w = ld_relaxed(slot);
+    if (w == 0ull)
+      atomicOr(p.err, PE_ERR_TIMEOUT);  // never expected: the chunk was counted
+    else
+      acc = combine(acc, unpack_partial(w));
+    *slot = 0ull;
   }
   acc = warp_combine(acc);
   if (lane == 0) {
@@ -442,10 +480,10 @@ __device__ __forceinline__ void stats_finish(const SampledParams& p, int vr, int
       const int x = __ldg(p.tokens + b * (p.Kp + 1) + j + 1);
       p.prob[vr] = (x >= 0 && x < p.V) ? ex2(E::at(rowp, x) * p.c2 - L) : -1.f;
     }
-    __threadfence();
+    fence_acq_rel();  // release
     if (atomicAdd(p.qcount + b, 1u) == (unsigned)(2 * p.Kp)) {  // all 2Kp+1 rows
       p.qcount[b] = 0u;
-      __threadfence();
+      fence_acq_rel();  // acquire: every row's probability
       decide(p, b);
     }
   }
@@ -573,11 +611,12 @@ __device__ __forceinline__ void residual_unit(const SampledParams& p, int u, int
   int last = 0;
   if (lane == 0) {
     if (draw) atomicMax(p.rkey + b, k);
-    __threadfence();
+    fence_acq_rel();  // release
     last = atomicAdd(p.dcount + b, 1u) == (unsigned)(p.C2 - 1);  // every unit of b is done
+    if (last) fence_acq_rel();  // acquire
   }
   if (!__shfl_sync(0xffffffffu, last, 0)) return;
-  __threadfence();
+  __syncwarp();
   int fallback = 0;
   if (lane == 0) {
     p.dcount[b] = 0u;
@@ -621,8 +660,9 @@ __global__ void __launch_bounds__(kThreads, 4) sampled_residual_kernel(const Sam
     u = __shfl_sync(0xffffffffu, next, 0);
   }
   if (lane == 0) {
-    __threadfence();
+    fence_acq_rel();  // release
     if (atomicAdd(p.sched + 3, 1u) == gridDim.x * kWarps - 1) {  // every other warp has left
+      fence_acq_rel();  // acquire: their reads of the list come first
       const unsigned listed = p.sched[4];
       for (unsigned k = 0; k < listed; ++k) p.rlist[k] = 0;
       atomicExch(p.sched + 2, 0u);
@@ -738,7 +778,7 @@ int pe_verify_sampled(const void* target_logits, const void* draft_logits, int d
   const SampledLayout L(B, Kp);
   char* w = static_cast<char*>(workspace);
   p.sched = reinterpret_cast<uint32_t*>(w);
-  p.partial = reinterpret_cast<float2*>(w + L.partial_off);
+  p.partial = reinterpret_cast<unsigned long long*>(w + L.partial_off);
   p.lse = reinterpret_cast<float*>(w + L.lse_off);
   p.prob = reinterpret_cast<float*>(w + L.prob_off);
   p.rcount = reinterpret_cast<uint32_t*>(w + L.rcount_off);

@@ -316,14 +316,15 @@ __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedStat
   }
   if (tid == 0) {
     const bool mine = (old & kXferCount) == (unsigned long long)nr;
-    if (mine) atomicExch(p.xfer + b, 0ull);  // both sides are done: clear for the next call
+    if (mine) {
+      atomicExch(p.xfer + b, 0ull);  // both sides are done: clear for the next call
+      fence_acq_rel();  // acquire: the tiles' writes of the row come before ours
+    }
     sh.xwrite = mine ? 1 : 0;
   }
   S::sync();
   if (sh.xwrite && PE_INVARIANT(p.err, oo + s >= 0 && oo + s < p.T)) {
-    // every default write of this row happened before the tiles' counts
     uint4* dst = p.X + (long long)(oo + s) * 2 * p.nvh;
-    __threadfence();  // acquire side of the hand-off, before the stores
     if (tid < p.nvh) dst[tid] = x1;
     if (kThreads + tid < p.nvh) dst[kThreads + tid] = x2;
     for (int v = 2 * kThreads + tid; v < p.nvh; v += kThreads)
@@ -448,18 +449,17 @@ __device__ __forceinline__ void finish_argmax_unit(const StepParams& p, SharedSt
     k = warp_max_key(k);
     if (tid == 0) {
       atomicMax(p.keys + r, k);
-      __threadfence();
+      fence_acq_rel();  // release
       const int b = r / (p.Kp + 1);
       const unsigned done = atomicAdd(p.count + b, 1u);
-      sh.last = (done == (unsigned)((p.Kp + 1) * p.C - 1)) ? b : -1;
+      const bool last = done == (unsigned)((p.Kp + 1) * p.C - 1);
+      if (last) fence_acq_rel();  // acquire: every chunk of the request is in
+      sh.last = last ? b : -1;
     }
   }
   S::sync();
   const int last = sh.last;
-  if (last >= 0) {
-    __threadfence();
-    request_epilogue<S>(p, sh, last);
-  }
+  if (last >= 0) request_epilogue<S>(p, sh, last);
 }
 
 // ------------------------------------------------------- early-exit units
@@ -530,7 +530,7 @@ __device__ __forceinline__ void argmax_unit_early(const StepParams& p, SharedSta
     if (tid == 0) {
       int due = -1, a = -1;
       atomicMax(p.keys + r, k);
-      __threadfence();
+      fence_acq_rel();  // release
       if (atomicAdd(p.rcount + r, 1u) == (unsigned)(p.C - 1)) {  // row r complete
         const unsigned long long kk = atomicExch(p.keys + r, 0ull);
         atomicExch(p.rcount + r, 0u);
@@ -540,10 +540,11 @@ __device__ __forceinline__ void argmax_unit_early(const StepParams& p, SharedSta
         const int vb = seg_begin(p, b + 1) - io - 1 - p.Kp;
         const bool match = j < p.Kp && am == __ldg(p.in_tokens + io + vb + j + 1);
         const unsigned long long bits = (1ull << j) | (match ? (1ull << (32 + j)) : 0ull);
-        __threadfence();  // the row's argmax is visible before its done bit
+        fence_acq_rel();  // release: the row's argmax before its done bit
         const unsigned long long old = atomicOr(p.state + b, bits);
         const int a_new = settled(old | bits, p.Kp);
         if (settled(old, p.Kp) < 0 && a_new >= 0) {
+          fence_acq_rel();  // acquire: the argmax of every row it settles on
           due = b;
           a = a_new;
         }
@@ -555,10 +556,7 @@ __device__ __forceinline__ void argmax_unit_early(const StepParams& p, SharedSta
   __syncthreads();
   const int due = sh.last;
   const int a = sh.first;
-  if (due >= 0) {
-    __threadfence();
-    request_epilogue<SyncAll, true>(p, sh, due, a);
-  }
+  if (due >= 0) request_epilogue<SyncAll, true>(p, sh, due, a);
 }
 
 // ------------------------------------------------------------------ X tiles
@@ -706,18 +704,19 @@ __device__ __forceinline__ void copy_unit(const StepParams& p, SharedState& sh, 
   }
   if (!vtile) return;
   // Hand-off: count this tile's verified rows into their requests' words,
-  // after every thread's stores of the tile are visible device-wide.  The
-  // tile that completes a request's count after its verdict was taken
-  // writes the bonus row (its embedding half with the bonus token); if the
-  // verdict comes later, the verdict writes it.
-  __threadfence();
+  // ordered after every thread's stores of the tile (the barrier gathers
+  // them, the counting thread's release fence publishes them).  The tile
+  // that completes a request's count after its verdict was taken writes the
+  // bonus row (its embedding half with the bonus token); if the verdict
+  // comes later, the verdict writes it.
   S::sync();
   if (tid < nrows && sh.vreq[tid] >= 0) {
     const int b = sh.vreq[tid];
+    fence_acq_rel();  // release
     const unsigned long long old = atomicAdd(p.xfer + b, 1ull);
     if ((old & kXferCount) + 1 == (unsigned long long)(p.Kp + 1) && (old & kXferVerdict)) {
       atomicExch(p.xfer + b, 0ull);  // both sides are done: clear for the next call
-      __threadfence();
+      fence_acq_rel();  // acquire: other tiles' writes of the row come first
       const int e = atomicAdd(&sh.nbonus, 1);
       sh.brow[e] = sh.vrow0[tid] + (int)((old >> 17) & 0xffull);
       sh.btok[e] = (int)(uint32_t)(old >> 32);
@@ -824,13 +823,13 @@ __global__ void __launch_bounds__(kThreads, 4) step_kernel_early(const StepParam
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    __threadfence();
+    fence_acq_rel();  // release
     const unsigned done = atomicAdd(p.sched + 1, 1u);
     sh.last = done == gridDim.x - 1;  // every other CTA has left
+    if (sh.last) fence_acq_rel();  // acquire: their last accesses come first
   }
   __syncthreads();
   if (sh.last) {  // the last CTA clears partly read rows, states and row results
-    __threadfence();
     for (int i = threadIdx.x; i < p.Rl; i += kThreads) {
       p.keys[i] = 0ull;
       p.rcount[i] = 0u;
@@ -1025,7 +1024,7 @@ __global__ void __launch_bounds__(kTmaThreads, MINB) step_kernel_tma(const StepP
   }
   __syncthreads();
   if (tid == 0) {
-    __threadfence();
+    fence_acq_rel();  // release
     const unsigned done = atomicAdd(p.sched + 1, 1u);
     if (done == gridDim.x - 1) {
       atomicExch(p.sched, 0u);
