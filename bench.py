@@ -10,7 +10,9 @@ target is stated).  Prints ONE JSON line on rank 0.
 
 Timing: W untimed steps, then K steps, each bracketed by CUDA events on the
 launching stream; between steps the L2 is flushed by writing a buffer of
-twice its size (outside the events).  Multi-GPU (torchrun): every rank runs
+twice its size (outside the events; --l2-flush write-read adds a read of
+another such buffer, so that no dirty line of the flush is left for the step
+to write back).  Multi-GPU (torchrun): every rank runs
 its own independent requests (weak scaling, no collective on the data path);
 the step time is the max over ranks.
 """
@@ -268,15 +270,46 @@ def cpu_model() -> str:
 
 # ------------------------------------------------------------ arms
 
-def config_of(spec, extra=None) -> dict:
+def config_of(spec, extra=None, l2_mode="write") -> dict:
     c = {"workload": spec.name, "description": spec.description, "B": spec.B,
          "Kp": spec.Kp, "K": spec.K, "H": spec.H, "V": spec.V,
          "dtype": str(spec.dtype).replace("torch.", ""),
-         "l2": "flushed between timed steps (write of 2x L2)",
+         "l2": L2Flush.describe_mode(l2_mode),
          "parallelism": "requests sharded across ranks, no data-path collective"}
     if extra:
         c.update(extra)
     return c
+
+
+class L2Flush:
+    """Evicts the L2 between timed steps, outside the events.  "write" (the
+    default) writes a buffer twice the L2's size.  That leaves the L2 full of
+    the flush's dirty lines, which the next step then writes back to HBM
+    while it streams (about 6 us of a B=256 step).  "write-read" follows the
+    write with a read of another such buffer, so no dirty line is left and
+    the step is timed on a clean, cold L2."""
+
+    def __init__(self, device, mode="write"):
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size
+        self.mode = mode
+        self.buf = torch.empty(2 * l2, dtype=torch.uint8, device=device)
+        if mode == "write-read":
+            self.rbuf = torch.ones(2 * l2 // 4, dtype=torch.float32, device=device)
+            self.acc = torch.empty((), dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.buf.zero_()
+        if self.mode == "write-read":
+            torch.sum(self.rbuf, dim=0, out=self.acc)
+
+    @staticmethod
+    def describe_mode(mode: str) -> str:
+        if mode == "write-read":
+            return "flushed between timed steps (write of 2x L2, then a read of 2x L2)"
+        return "flushed between timed steps (write of 2x L2)"
+
+    def describe(self) -> str:
+        return self.describe_mode(self.mode)
 
 
 def run_reference(args):
@@ -331,8 +364,7 @@ def run_ours(args):
     w = wl.make_workload(spec, rank_seed(args.workload, rank), device=device)
     out, ws, err = harness.allocate(w, device)
     packed = harness.pack(w, out, ws, err)
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    flush = torch.empty(2 * l2, dtype=torch.uint8, device=device)
+    flush = L2Flush(device, args.l2_flush)
     stream = torch.cuda.current_stream(device)
 
     run_step = _native.step_early_exit_packed if args.early_exit else _native.step_packed
@@ -341,7 +373,7 @@ def run_ours(args):
         run_step(packed, stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize(device)
     if int(err.item()) != 0:
@@ -355,7 +387,7 @@ def run_ours(args):
     t_wall0 = time.time()
     torch.cuda.nvtx.range_push("timed")
     for e0, e1 in ev:
-        flush.zero_()
+        flush()
         e0.record(stream)
         step()
         e1.record(stream)
@@ -410,7 +442,7 @@ def run_ours(args):
                                        "min_us": min(step_ms) * 1e3,
                                        "p99_us": sorted(step_ms)[int(0.99 * (len(step_ms) - 1))] * 1e3,
                                        "max_us": max(step_ms) * 1e3,
-                                       "tuning": _native.get_tuning()}),
+                                       "tuning": _native.get_tuning()}, l2_mode=flush.mode),
             "us_per_step": mean_ms_max * 1e3,
             "hbm_gbs": achieved,
             "roofline": roofline,
@@ -461,8 +493,7 @@ def run_sampled(args):
     bon = torch.empty(B, dtype=torch.int32, device=device)
     ws = torch.zeros(_native.workspace_bytes_sampled(B, Kp), dtype=torch.uint8, device=device)
     err = _native.new_error_word(device)
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    flush = torch.empty(2 * l2, dtype=torch.uint8, device=device)
+    flush = L2Flush(device, args.l2_flush)
     stream = torch.cuda.current_stream(device)
     T = args.temperature
 
@@ -471,7 +502,7 @@ def run_sampled(args):
                                1234 + rank, acc, bon, ws, err, stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize(device)
     if int(err.item()) != 0 or int(ws.count_nonzero()) != 0:
@@ -484,7 +515,7 @@ def run_sampled(args):
     t_wall0 = time.time()
     torch.cuda.nvtx.range_push("timed")
     for e0, e1 in ev:
-        flush.zero_()
+        flush()
         e0.record(stream)
         step()
         e1.record(stream)
@@ -535,7 +566,7 @@ def run_sampled(args):
                                    "T=%g" % (B, Kp, V, T),
                        "accepted_len_histogram": torch.bincount(
                            acc.long().cpu(), minlength=Kp + 1).tolist(),
-                       "l2": "flushed between steps (2x L2 written)",
+                       "l2": flush.describe(),
                        "median_us": statistics.median(step_ms) * 1e3,
                        "min_us": min(step_ms) * 1e3},
             "us_per_step": mean_ms_max * 1e3,
@@ -577,15 +608,14 @@ def run_readout(args):
     out = torch.empty(n, dtype=torch.int32, device=device)
     ws = _native.new_workspace(n, n, device)
     err = _native.new_error_word(device)
-    l2 = torch.cuda.get_device_properties(device).L2_cache_size
-    flush = torch.empty(2 * l2, dtype=torch.uint8, device=device)
+    flush = L2Flush(device, args.l2_flush)
     stream = torch.cuda.current_stream(device)
 
     def step():
         _native.draft_readout(logits, out, ws, err, None, stream)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize(device)
     if int(err.item()) != 0 or int(ws.count_nonzero()) != 0:
@@ -598,7 +628,7 @@ def run_readout(args):
     t_wall0 = time.time()
     torch.cuda.nvtx.range_push("timed")
     for e0, e1 in ev:
-        flush.zero_()
+        flush()
         e0.record(stream)
         step()
         e1.record(stream)
@@ -636,7 +666,7 @@ def run_readout(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "bf16", "data": "synthetic",
             "config": {"workload": "greedy drafter readout B=%d K=%d V=%d bf16" % (B, K, V),
-                       "l2": "flushed between steps (2x L2 written)",
+                       "l2": flush.describe(),
                        "median_us": statistics.median(step_ms) * 1e3,
                        "min_us": min(step_ms) * 1e3,
                        "tuning": _native.get_tuning()},
@@ -751,6 +781,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=list(wl.SPECS), default="decode_b256")
     ap.add_argument("--tuning", default="", help="JSON launch-shape knobs")
+    ap.add_argument("--l2-flush", choices=["write", "write-read"], default="write",
+                    help="how the L2 is evicted between timed steps (see L2Flush)")
     ap.add_argument("--graph", type=int, default=0,
                     help="also time N steps captured in one CUDA graph")
     ap.add_argument("--early-exit", action="store_true",
