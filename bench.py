@@ -39,6 +39,7 @@ import torch  # noqa: E402
 from speculative_decoding_pe_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "verify+rebuild+assemble draft rows/s"
+DTYPE_NAME = {torch.bfloat16: "bf16", torch.float32: "f32"}  # the JSON line's "dtype"
 UNIT = "rows/s"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("speculative_decoding_pe_gb300/csrc/pe_step.cu",
@@ -335,7 +336,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype":
-        str(spec.dtype).replace("torch.", ""), "data": "synthetic",
+        DTYPE_NAME[spec.dtype], "data": "synthetic",
         "config": config_of(spec),
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": "first %d of %d requests per step (%d draft rows), "
@@ -434,7 +435,7 @@ def run_ours(args):
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": mean_ms_max,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-            "dtype": str(spec.dtype).replace("torch.", ""), "data": "synthetic",
+            "dtype": DTYPE_NAME[spec.dtype], "data": "synthetic",
             "config": config_of(spec, {"T_per_rank": T, "R_per_rank": w.R,
                                        "early_exit": bool(args.early_exit),
                                        "logits_rows_needed": needed,
