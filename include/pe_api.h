@@ -162,9 +162,11 @@ size_t pe_workspace_bytes_sampled(int32_t B, int32_t Kp);
  *                [B*Kp] fp32 in [0,1).  Both may be NULL when Kp == 0.
  *  temperature   > 0 (PE_EINVAL otherwise); logits must be finite.
  *  workspace     pe_workspace_bytes_sampled(B, Kp) bytes, zeroed.
- *  err           device error word (no bits are defined for this call).
- * Arithmetic is fp32 (exp and log of CUDA's fast intrinsics for the
- * probabilities, logf for the noise): accept decisions and draws agree with
+ *  err           device error word: PE_ERR_TIMEOUT when a bounded wait of
+ *                the statistics merge gave up (never expected).
+ * Arithmetic is fp32 in the log2 domain (the hardware's approximate ex2 and
+ * lg2 instructions; near U = 1 the noise uses a short series of
+ * -log2(1 - t) instead): accept decisions and draws agree with
  * an exact evaluation except where p(x) - u q(x), or the gap between the
  * two best Gumbel scores, is within rounding of zero.  Two kernel launches;
  * B == 0 enqueues nothing. */
