@@ -673,7 +673,8 @@ def run_readout(args):
                        "tuning": _native.get_tuning()},
             "us_per_step": mean_ms_max * 1e3,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                         "frac": achieved / peak, "traffic": None,
+                         "frac": achieved / peak,
+                         "traffic": profiled_traffic("decode_b256", "pe_draft_readout"),
                          "peak_source": peak_kind, "algorithmic_bytes_per_launch": total,
                          "kernel": "pe::step_kernel<bf16> (readout: argmax units only)"},
             "cpu_baseline": cpu, "gpu_launches": args.steps, "clocks": clocks}))
