@@ -47,8 +47,7 @@ struct SampledParams {
   int32_t* bonus_token;
   uint32_t* err;
   // workspace
-  uint32_t* sched;            // [8] [0] stats unit counter; [2], [3] residual unit
-                              // counter and warps done;
+  uint32_t* sched;            // [8] [0] stats unit counter; [3] residual warps done;
                               // [4]: requests listed for a residual draw
   unsigned long long* partial;  // [Rt+Rd][kMaxChunksSampled] (max, sum) per chunk,
                                 // packed by pack_partial (0: not yet written)
@@ -641,23 +640,19 @@ __device__ __forceinline__ void residual_unit(const SampledParams& p, int u, int
   }
 }
 
-// Persistent warps over the residual units of the listed requests
-// (sched[2]: unit counter, sched[3]: warps done); the list is complete, the
-// stats pass having finished.  The last warp to leave clears the list and
-// the counter words.
+// Persistent warps over the residual units of the listed requests, handed
+// out statically (warp w takes units w, w + warps, ...: the units are all
+// the same size, so a work counter would only add same-address atomics);
+// the list is complete, the stats pass having finished.  The last warp to
+// leave (sched[3]: warps done) clears the list and the counter words.
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 4) sampled_residual_kernel(const SampledParams p) {
   const int lane = threadIdx.x & 31;
   const int n_units = (int)__ldcg(p.sched + 4) * p.C2;
-  int u = 0;
-  if (lane == 0) u = (int)atomicAdd(p.sched + 2, 1u);
-  u = __shfl_sync(0xffffffffu, u, 0);
-  while (u < n_units) {
-    int next = 0;
-    if (lane == 0) next = (int)atomicAdd(p.sched + 2, 1u);
+  const int nw = gridDim.x * kWarps;
+  for (int u = blockIdx.x * kWarps + (threadIdx.x >> 5); u < n_units; u += nw) {
     const int k = u / p.C2;
     residual_unit<DT>(p, __ldcg(p.rlist + k) * p.C2 + (u - k * p.C2), lane);
-    u = __shfl_sync(0xffffffffu, next, 0);
   }
   if (lane == 0) {
     fence_acq_rel();  // release
@@ -665,7 +660,6 @@ __global__ void __launch_bounds__(kThreads, 4) sampled_residual_kernel(const Sam
       fence_acq_rel();  // acquire: their reads of the list come first
       const unsigned listed = p.sched[4];
       for (unsigned k = 0; k < listed; ++k) p.rlist[k] = 0;
-      atomicExch(p.sched + 2, 0u);
       atomicExch(p.sched + 3, 0u);
       atomicExch(p.sched + 4, 0u);
     }

@@ -206,13 +206,45 @@ def pin_sampled_preserves_target_distribution():
     u = torch.tensor(rng.random(N), dtype=torch.float32)
     acc, bon = oracle.verify_sampled(t, d, N, 1, tokens, u, 1.0, 2024)
     acc, bon = acc.numpy(), bon.numpy()
+    assert ((acc >= 0) & (acc <= 1)).all() and ((bon >= 0) & (bon < V)).all()
     first = np.where(acc >= 1, x, bon)
     assert _chi2(np.bincount(first, minlength=V), p0) < 16.27
     after = bon[acc == 1]
     assert _chi2(np.bincount(after, minlength=V), p1) < 16.27
     # a plain draw (no drafts) is distributed as p_0 too
     acc0, bon0 = oracle.verify_sampled(t[0::2].contiguous(), None, N, 0, None, None, 1.0, 99)
+    assert ((bon0 >= 0) & (bon0 < V)).all()
     assert _chi2(np.bincount(bon0.numpy(), minlength=V), p0) < 16.27
+
+
+def pin_sampled_residual_across_chunks():
+    """The same guarantee on a wide row whose support is four far-apart
+    columns (0, 2048, 1, 2049: the residual weight 0.2 and 0.3 sits in
+    columns 1 and 2049, the other two cancel), so that any per-chunk or
+    per-column bookkeeping of the draw is exercised: the first emitted
+    token must follow p_0 over those columns (chi-square, 3 degrees of
+    freedom, 99.9 % quantile 16.27, over 4000 requests)."""
+    rng = np.random.default_rng(29)
+    N, V = 4000, 4096
+    cols = np.array([0, 2048, 1, 2049])  # entries of p0 / q0 -> columns
+    p0 = np.array([0.1, 0.2, 0.3, 0.4])
+    p1 = np.array([0.4, 0.3, 0.2, 0.1])
+    q0 = np.array([0.4, 0.4, 0.1, 0.1])
+    t = torch.full((2 * N, V), -1.0e4, dtype=torch.float32)
+    t[0::2, cols] = torch.tensor(np.log(p0), dtype=torch.float32)
+    t[1::2, cols] = torch.tensor(np.log(p1), dtype=torch.float32)
+    d = torch.full((N, V), -1.0e4, dtype=torch.float32)
+    d[:, cols] = torch.tensor(np.log(q0), dtype=torch.float32)
+    x = cols[rng.choice(4, size=N, p=q0)]
+    tokens = torch.zeros(2 * N, dtype=torch.int32)
+    tokens[1::2] = torch.tensor(x, dtype=torch.int32)
+    u = torch.tensor(rng.random(N), dtype=torch.float32)
+    acc, bon = oracle.verify_sampled(t, d, N, 1, tokens, u, 1.0, 31)
+    acc, bon = acc.numpy(), bon.numpy()
+    first = np.where(acc >= 1, x, bon)
+    assert np.isin(first, cols).all()
+    counts = np.array([(first == c).sum() for c in cols])
+    assert _chi2(counts, p0) < 16.27
 
 
 # -------------------------------------------------- rebuild invariants (a3-a5)
@@ -457,6 +489,7 @@ def pin_error_rules():
 ALL_PINS = [pin_argmax_bruteforce, pin_argmax_numpy, pin_draft_readout,
             pin_philox_known_answers, pin_sampled_cold_is_greedy,
             pin_sampled_same_distribution_accepts_all,
-            pin_sampled_preserves_target_distribution, pin_accept_enumeration,
+            pin_sampled_preserves_target_distribution, pin_sampled_residual_across_chunks,
+            pin_accept_enumeration,
             pin_planted, pin_step_invariants, pin_golden_decode,
             pin_golden_prefill, pin_error_rules]

@@ -216,6 +216,37 @@ def test_sampled_preserves_target_distribution():
     assert _chi2(np.bincount(bon0.numpy(), minlength=V), p0) < 16.27
 
 
+def test_sampled_residual_across_chunks():
+    """A wide row whose support is four far-apart columns (the residual
+    weight 0.2 and 0.3 sits in columns 1 and 2049, in different residual
+    units): the first emitted token must still follow p_0 over them, and
+    every request equals the oracle up to explained near ties."""
+    rng = np.random.default_rng(31)
+    N, V = 4000, 4096
+    cols = np.array([0, 2048, 1, 2049])
+    p0 = np.array([0.1, 0.2, 0.3, 0.4])
+    p1 = np.array([0.4, 0.3, 0.2, 0.1])
+    q0 = np.array([0.4, 0.4, 0.1, 0.1])
+    t = torch.full((2 * N, V), -1.0e4, dtype=torch.float32)
+    t[0::2, cols] = torch.tensor(np.log(p0), dtype=torch.float32)
+    t[1::2, cols] = torch.tensor(np.log(p1), dtype=torch.float32)
+    d = torch.full((N, V), -1.0e4, dtype=torch.float32)
+    d[:, cols] = torch.tensor(np.log(q0), dtype=torch.float32)
+    x = cols[rng.choice(4, size=N, p=q0)]
+    tokens = torch.zeros(2 * N, dtype=torch.int32)
+    tokens[1::2] = torch.tensor(x, dtype=torch.int32)
+    u = torch.tensor(rng.random(N), dtype=torch.float32)
+    s = wl.SampledInputs(B=N, Kp=1, V=V, target_logits=t, draft_logits=d, tokens=tokens,
+                         u_accept=u)
+    got = run_gpu(s, 1.0, 4343)
+    assert_parity(s, 1.0, 4343, got, run_oracle(s, 1.0, 4343))
+    acc, bon = got[0].numpy(), got[1].numpy()
+    first = np.where(acc >= 1, x, bon)
+    assert np.isin(first, cols).all()
+    counts = np.array([(first == c).sum() for c in cols])
+    assert _chi2(counts, p0) < 16.27
+
+
 def test_sampled_workspace_reuse_and_determinism():
     big = wl.make_sampled_inputs(64, 7, 20011, dtype=torch.bfloat16, seed=13)
     small = wl.make_sampled_inputs(5, 2, 999, dtype=torch.float32, seed=14)
