@@ -47,8 +47,8 @@ struct SampledParams {
   int32_t* bonus_token;
   uint32_t* err;
   // workspace
-  uint32_t* sched;            // [8] [0] stats unit counter; [3] residual warps done;
-                              // [4]: requests listed for a residual draw
+  uint32_t* sched;            // [3] residual warps done; [4] requests listed for a
+                              // residual draw; [8 + 64 i] stats unit counter i
   unsigned long long* partial;  // [Rt+Rd][kMaxChunksSampled] (max, sum) per chunk,
                                 // packed by pack_partial (0: not yet written)
   float* lse;                 // [Rt+Rd] log2 of the row's normaliser (log2 domain)
@@ -505,16 +505,35 @@ __device__ __forceinline__ void stats_unit(const SampledParams& p, int u, int la
   stats_finish<DT>(p, vr, c, lane, m, s, best);
 }
 
-// Persistent warps over a dynamic unit counter (sched[0]); the next unit is
-// fetched before the current one is processed.  Every warp takes exactly one
-// index past the last unit and then no other, so the warp that receives the
-// last such index (n_units + warps - 1) resets the counter.
+// Persistent warps over dynamic unit counters; the next unit is fetched
+// before the current one is processed.  Counter i (kStatsCounters of them,
+// 256 bytes apart in the workspace) hands out units i, i + k, i + 2k, ...,
+// so each counter word takes half the claims: one word for all ~4900 warps
+// measured slower on some GPUs (its atomics queue).  A warp draws from its
+// own counter, then from the other, each until it runs out, so every warp
+// makes exactly one failing claim on every counter, and the claim that
+// returns a counter's last position (its units plus one per warp) resets it.
 constexpr int kStatsCtasPerSm = 4;  // 32 warps per SM: 64 registers a thread
+constexpr int kStatsCounters = 2;
+constexpr int kCounterWords = 64;   // words between counters
 
-__device__ __forceinline__ int stats_claim(const SampledParams& p, int n_units) {
-  const unsigned v = atomicAdd(p.sched, 1u);
-  if (v == (unsigned)n_units + gridDim.x * kWarps - 1u) atomicExch(p.sched, 0u);
-  return (int)v;
+__device__ __forceinline__ uint32_t* stats_counter(const SampledParams& p, int i) {
+  return p.sched + 8 + i * kCounterWords;
+}
+
+// Next unit for this warp (lane 0), or n_units once every counter ran out.
+__device__ __forceinline__ int stats_next(const SampledParams& p, int n_units, int& ci,
+                                          int& ndone) {
+  while (ndone < kStatsCounters) {
+    const int n_i = (n_units - ci + kStatsCounters - 1) / kStatsCounters;
+    uint32_t* ctr = stats_counter(p, ci);
+    const unsigned v = atomicAdd(ctr, 1u);
+    if (v == (unsigned)n_i + gridDim.x * kWarps - 1u) atomicExch(ctr, 0u);
+    if ((int)v < n_i) return ci + (int)v * kStatsCounters;
+    ++ndone;
+    ci = ci + 1 == kStatsCounters ? 0 : ci + 1;
+  }
+  return n_units;
 }
 
 template <int DT>
@@ -522,12 +541,13 @@ __global__ void __launch_bounds__(kThreads, kStatsCtasPerSm) sampled_stats_kerne
     const SampledParams p) {
   const int lane = threadIdx.x & 31;
   const int n_units = (p.Rt + p.Rd) * p.C;
+  int ci = (blockIdx.x * kWarps + (threadIdx.x >> 5)) % kStatsCounters, ndone = 0;
   int u = 0;
-  if (lane == 0) u = stats_claim(p, n_units);
+  if (lane == 0) u = stats_next(p, n_units, ci, ndone);
   u = __shfl_sync(0xffffffffu, u, 0);
   while (u < n_units) {
     int next = 0;
-    if (lane == 0) next = stats_claim(p, n_units);
+    if (lane == 0) next = stats_next(p, n_units, ci, ndone);
     stats_unit<DT>(p, u, lane);
     u = __shfl_sync(0xffffffffu, next, 0);
   }
@@ -676,7 +696,8 @@ struct SampledLayout {
       rkey_off, rlist_off, bytes;
   SampledLayout(long long B, long long Kp) {
     const long long rows = B * (Kp + 1) + B * Kp;
-    size_t o = 32;  // eight scheduler words
+    // eight scheduler words, then the stats counters 256 bytes apart
+    size_t o = 32 + 4 * pe::kCounterWords * pe::kStatsCounters;
     auto take = [&](size_t n, size_t align) {
       o = (o + align - 1) / align * align;
       const size_t at = o;
