@@ -284,10 +284,12 @@ int pe_step(const pe_step_args* args /* host */, void* stream);
  * earlier mismatch is skipped).  Every output equals pe_step's, except
  * target_argmax, which holds each request's rows 0..a_b and -1 for the rows
  * after a_b.  Same arguments and workspace as pe_step; Kp <= 31 (one bit per
- * verified row), else PE_EINVAL.  Always runs the register-streaming kernel
+ * verified row), else PE_EINVAL.  Runs the register-streaming kernel
  * (pe_tuning.variant does not apply).  It pays off when many requests share
- * the step (their rows interleave); with one or a few requests the rows of a
- * request serialise and the full-read pe_step is faster. */
+ * the step (their rows interleave); with few requests the rows of a request
+ * serialise, so when the logits take at most pe_tuning.early_full_read_mb
+ * MiB (default 128) this call reads every row instead, with the same
+ * outputs (target_argmax still -1 after a_b). */
 int pe_step_early_exit(const pe_step_args* args /* host */, void* stream);
 
 /* pe_step for callers that cannot allocate device memory at all, not even
@@ -327,6 +329,12 @@ typedef struct pe_tuning {
                               the argmax chunks, then the other copy tiles
                               (same outputs; the verdict usually writes the
                               bonus row) */
+  int32_t early_full_read_mb; /* pe_step_early_exit reads every row (the
+                              full-read kernel, outputs unchanged) when the
+                              logits take at most this many MiB: with few
+                              requests the serial row waves cost more than
+                              the extra bytes.  Default 128; -1 sets 0
+                              (always the early-exit kernel) */
 } pe_tuning;
 int pe_get_tuning(pe_tuning* out /* host */);
 int pe_set_tuning(const pe_tuning* in /* host */);

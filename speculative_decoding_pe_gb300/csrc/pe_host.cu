@@ -16,6 +16,7 @@ std::atomic<int> g_chunk_batches{3};
 std::atomic<int> g_rows_per_unit{4};
 std::atomic<int> g_variant{1};
 std::atomic<int> g_queue_order{2};
+std::atomic<int> g_early_full_read_mb{128};
 }  // namespace
 
 int device_info(DeviceInfo* out) {
@@ -40,6 +41,7 @@ Tuning tuning() {
   t.rows_per_unit = g_rows_per_unit.load(std::memory_order_relaxed);
   t.variant = g_variant.load(std::memory_order_relaxed);
   t.queue_order = g_queue_order.load(std::memory_order_relaxed);
+  t.early_full_read_mb = g_early_full_read_mb.load(std::memory_order_relaxed);
   return t;
 }
 
@@ -60,6 +62,7 @@ int pe_get_tuning(pe_tuning* out) {
   out->rows_per_unit = t.rows_per_unit;
   out->variant = t.variant;
   out->queue_order = t.queue_order;
+  out->early_full_read_mb = t.early_full_read_mb;
   return PE_OK;
 }
 
@@ -71,11 +74,13 @@ int pe_set_tuning(const pe_tuning* in) {
     return PE_EINVAL;
   if (in->variant < 0 || in->variant > 2) return PE_EINVAL;
   if (in->queue_order < 0 || in->queue_order > 2) return PE_EINVAL;
+  if (in->early_full_read_mb < -1 || in->early_full_read_mb > 65536) return PE_EINVAL;
   if (in->ctas_per_sm) pe_host::g_ctas_per_sm.store(in->ctas_per_sm);
   if (in->chunk_batches) pe_host::g_chunk_batches.store(in->chunk_batches);
   if (in->rows_per_unit) pe_host::g_rows_per_unit.store(in->rows_per_unit);
   if (in->variant) pe_host::g_variant.store(in->variant);
   if (in->queue_order) pe_host::g_queue_order.store(in->queue_order);
+  if (in->early_full_read_mb) pe_host::g_early_full_read_mb.store(in->early_full_read_mb < 0 ? 0 : in->early_full_read_mb);
   return PE_OK;
 }
 

@@ -139,6 +139,7 @@ struct Tuning {
   int rows_per_unit;
   int variant;
   int queue_order;
+  int early_full_read_mb;
 };
 Tuning tuning();
 

@@ -59,6 +59,7 @@ struct StepParams {
   int chunk_vecs, C, Rl;  // argmax chunking: vectors per chunk, chunks per row, rows
   int n_arg_units, rows_per_unit, n_copy_units, n_units;
   int rv, n_vtile;        // verified rows B(K'+1); copy tiles over them
+  int mask_unread;        // target_argmax -1 after a_b (early exit served by a full read)
   int vfirst;             // 1: those tiles are handed out before the argmax chunks
   const void* logits;
   const int32_t* row_index;  // logits row of argmax row r (NULL: r itself)
@@ -238,9 +239,10 @@ __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedStat
   S::sync();
   // accepted length: first draft that differs from the target's choice
   if (!EARLY && tid < Kp && sh.amax[tid] != sh.tok[tid]) atomicMin(&sh.first, tid);
-  if (p.target_argmax && tid < nr) p.target_argmax[(long long)b * nr + tid] = sh.amax[tid];
   S::sync();
   const int a = sh.first;
+  if (p.target_argmax && tid < nr)
+    p.target_argmax[(long long)b * nr + tid] = p.mask_unread && tid > a ? -1 : sh.amax[tid];
   const int bonus = sh.amax[a];
   if (!p.full) {
     if (tid == 0) {
@@ -1301,6 +1303,13 @@ int step_common(const pe_step_args* a, void* stream, bool early) {
   p.X = static_cast<uint4*>(a->X);
   p.err = a->err;
   const int rows = B * (Kp + 1);
+  // Early exit at a small logits footprint: reading every row is faster than
+  // the serial row waves (measured crossover ~125 MB); the outputs stay the
+  // early-exit ones (target_argmax -1 after a_b).
+  if (early && (long long)rows * p.row_bytes <= (long long)tn.early_full_read_mb << 20) {
+    early = false;
+    p.mask_unread = 1;
+  }
   // the early-exit step runs on the register-streaming kernel
   pe_host::Tuning tk = tn;
   if (early) tk.variant = 1;

@@ -168,5 +168,12 @@ def test_tuning_roundtrip(lib):
             _native.set_tuning(queue_order=3)
         _native.set_tuning(queue_order=2)
         assert _native.get_tuning()["queue_order"] == 2
+        _native.set_tuning(early_full_read_mb=64)
+        assert _native.get_tuning()["early_full_read_mb"] == 64
+        _native.set_tuning(early_full_read_mb=-1)  # -1 stores 0: always the early-exit kernel
+        assert _native.get_tuning()["early_full_read_mb"] == 0
+        with pytest.raises(_native.PEError):
+            _native.set_tuning(early_full_read_mb=-2)
     finally:
-        _native.set_tuning(**before)
+        _native.set_tuning(**{k: (v if v or k != "early_full_read_mb" else -1)
+                              for k, v in before.items()})

@@ -2,7 +2,10 @@
 
 Every output must equal the full step's bit for bit, except target_argmax:
 rows 0..a_b of each request carry their argmax, later rows -1 (they may
-never have been read)."""
+never have been read).  Every test runs twice: with the early-exit kernel
+forced, and with the default, under which small batches (logits of at most
+pe_tuning.early_full_read_mb MiB) are served by the full-read kernel with
+the same outputs."""
 import pytest
 import torch
 
@@ -20,6 +23,18 @@ def lib():
         pytest.skip("needs a CUDA GPU")
     build.build()
     return _native.load()
+
+
+def _restore(t):
+    _native.set_tuning(**{k: (v if v or k != "early_full_read_mb" else -1) for k, v in t.items()})
+
+
+@pytest.fixture(autouse=True, params=["early_kernel", "default"])
+def early_path(request):
+    before = _native.get_tuning()
+    _native.set_tuning(early_full_read_mb=-1 if request.param == "early_kernel" else 128)
+    yield request.param
+    _restore(before)
 
 
 def run_early(w, workspace=None):

@@ -57,7 +57,7 @@ def _spec(rng: random.Random, i: int) -> wl.WorkloadSpec:
 def _tuning(rng: random.Random) -> dict:
     return dict(ctas_per_sm=rng.choice([1, 2, 4]), chunk_batches=rng.choice([1, 2, 3, 4]),
                 rows_per_unit=rng.choice([1, 2, 3, 4, 8, 16]), variant=rng.choice([1, 1, 2]),
-                queue_order=rng.choice([1, 2]))
+                queue_order=rng.choice([1, 2]), early_full_read_mb=rng.choice([-1, 128]))
 
 
 def _run_early(w):
@@ -98,4 +98,5 @@ def test_fuzz(case):
                 assert torch.equal(ta[b, :a + 1], ra[b, :a + 1]), (what, b)
                 assert (ta[b, a + 1:] == -1).all(), (what, b)
     finally:
-        _native.set_tuning(**before)
+        _native.set_tuning(**{k: (v if v or k != "early_full_read_mb" else -1)
+                              for k, v in before.items()})
