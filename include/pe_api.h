@@ -284,8 +284,10 @@ int pe_step(const pe_step_args* args /* host */, void* stream);
  * earlier mismatch is skipped).  Every output equals pe_step's, except
  * target_argmax, which holds each request's rows 0..a_b and -1 for the rows
  * after a_b.  Same arguments and workspace as pe_step; Kp <= 31 (one bit per
- * verified row), else PE_EINVAL.  Runs the register-streaming kernel
- * (pe_tuning.variant does not apply).  It pays off when many requests share
+ * verified row), else PE_EINVAL.  The early-exit reading runs the
+ * register-streaming kernel (pe_tuning.variant does not apply; the full
+ * read below follows it, with the same outputs).  It pays off when many
+ * requests share
  * the step (their rows interleave); with few requests the rows of a request
  * serialise, so when the logits take at most pe_tuning.early_full_read_mb
  * MiB (default 128) this call reads every row instead, with the same
