@@ -284,14 +284,13 @@ int pe_step(const pe_step_args* args /* host */, void* stream);
  * earlier mismatch is skipped).  Every output equals pe_step's, except
  * target_argmax, which holds each request's rows 0..a_b and -1 for the rows
  * after a_b.  Same arguments and workspace as pe_step; Kp <= 31 (one bit per
- * verified row), else PE_EINVAL.  The early-exit reading runs the
- * register-streaming kernel (pe_tuning.variant does not apply; the full
- * read below follows it, with the same outputs).  It pays off when many
- * requests share
- * the step (their rows interleave); with few requests the rows of a request
+ * verified row), else PE_EINVAL.  It pays off when many requests share the
+ * step (their rows interleave); with few requests the rows of a request
  * serialise, so when the logits take at most pe_tuning.early_full_read_mb
  * MiB (default 128) this call reads every row instead, with the same
- * outputs (target_argmax still -1 after a_b). */
+ * outputs (target_argmax still -1 after a_b).  The early-exit reading runs
+ * the register-streaming kernel (pe_tuning.variant does not apply); the
+ * full read follows pe_tuning.variant. */
 int pe_step_early_exit(const pe_step_args* args /* host */, void* stream);
 
 /* pe_step for callers that cannot allocate device memory at all, not even
