@@ -1,6 +1,7 @@
 // Fused P-EAGLE drafting step on one GPU: greedy verification, draft-batch
 // rebuild and drafter input assembly in a single persistent launch
-// (pe_step), and verification alone (pe_verify_greedy).
+// (pe_step); the same with early exit (pe_step_early_exit); verification
+// alone (pe_verify_greedy); the drafter readout (pe_draft_readout).
 //
 // Sources (page title -- section):
 //  "P-EAGLE: Parallel Speculative Decoding in vLLM" -- Fused Triton Kernel
@@ -13,7 +14,9 @@
 //    vLLM" -- quick-read section: Input_1 = emb(new) (+) h_context,
 //    Input_i = emb(mask) (+) h_shared for 2 <= i <= K; acceptance length.
 //
-// Design (one launch, no grid-wide barrier, no spin-wait):
+// Design (one launch, no grid-wide barrier; the register-streaming kernel
+// has no spin-wait, the pipelined variant's waits on its own bulk-copy ring
+// are bounded):
 //  * A persistent grid pulls work units from a counter in the workspace.
 //    Units [0, n_arg) are argmax chunks (row r, chunk c) of the logits, in
 //    row order; units [n_arg, n_units) copy tiles of X rows, first those of
@@ -35,6 +38,12 @@
 //    tile comes second (one atomic each on the request's hand-off word)
 //    writes E[bonus] over the tile's default.  Every other byte of X has one
 //    writer.
+//  * Each CTA takes one index past the end of the queue and leaves; the
+//    claim that returns the last index resets the counter for the next call.
+//  * Early exit reads a request's rows in order and skips the rows after a
+//    known mismatch (step_kernel_early); with a small logits footprint the
+//    host serves it with the full read instead, the epilogue writing -1 to
+//    target_argmax after a_b.
 #include "pe_internal.cuh"
 #include "pe_tma.cuh"
 #include "pe_workspace.cuh"
