@@ -47,3 +47,14 @@ def test_early_exit_counts_needed_rows_only():
     early = bench.algorithmic_bytes(spec, 2048, logits_rows=729)
     assert full["logits"] - early["logits"] == (2048 - 729) * 151936 * 2
     assert early["hidden"] == full["hidden"] and early["X"] == full["X"]
+
+
+def test_sampled_bytes():
+    """Rejection sampling at B=256, K'=7, V=151936 bf16 with 141 requests
+    rejecting a draft: 3840 rows read once (1.1670 GB) plus the target and
+    draft row of each rejection again (85.7 MB): 1.253 GB with the tokens,
+    coins and outputs."""
+    got = bench.sampled_bytes(256, 7, 151936, 2, 141)
+    assert got["logits"] == (256 * 8 + 256 * 7) * 151936 * 2
+    assert got["residual_reread"] == 141 * 2 * 151936 * 2
+    assert abs(got["total"] - 1.2526e9) / 1.2526e9 < 0.001, got["total"]
