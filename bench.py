@@ -44,6 +44,7 @@ UNIT = "rows/s"
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ("speculative_decoding_pe_gb300/csrc/pe_step.cu",
                   "speculative_decoding_pe_gb300/csrc/pe_internal.cuh",
+                  "speculative_decoding_pe_gb300/csrc/pe_tma.cuh",
                   "speculative_decoding_pe_gb300/csrc/pe_workspace.cuh")
 SAMPLED_SOURCES = ("speculative_decoding_pe_gb300/csrc/pe_sampled.cu",
                    "speculative_decoding_pe_gb300/csrc/pe_internal.cuh")
@@ -174,7 +175,11 @@ def profiled_traffic(workload: str, kernel: str = "pe_step", sources=KERNEL_SOUR
 # ------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    """nvidia-smi samples of SM clock and throttle reasons while running.
+
+    Started before the warm-up (nvidia-smi takes a moment to print its first
+    sample); ``stop(t0, t1)`` keeps the samples taken between t0 and t1
+    (wall clock), waiting briefly for one past t1 to arrive."""
     QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,"
              "clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
              "clocks_event_reasons.hw_thermal_slowdown,"
@@ -191,9 +196,16 @@ class ClockSampler:
         except OSError:
             self.proc = None
 
+    @staticmethod
+    def _stamp(text: str) -> float:
+        whole, _, frac = text.strip().partition(".")
+        ts = time.mktime(time.strptime(whole, "%Y/%m/%d %H:%M:%S"))
+        return ts + (float("0." + frac) if frac.isdigit() else 0.0)
+
     def stop(self, t0: float, t1: float) -> dict:
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(max(0.0, min(0.5, t1 + 0.3 - time.time())))  # let a sample past t1 land
         self.proc.terminate()
         out, _ = self.proc.communicate(timeout=10)
         rows = []
@@ -201,12 +213,10 @@ class ClockSampler:
             if len(rec) < 10:
                 continue
             try:
-                ts = time.mktime(time.strptime(rec[0].strip().split(".")[0],
-                                               "%Y/%m/%d %H:%M:%S"))
-                rows.append((ts, [r.strip() for r in rec]))
+                rows.append((self._stamp(rec[0]), [r.strip() for r in rec]))
             except ValueError:
                 continue
-        inside = [r for ts, r in rows if t0 - 1.0 <= ts <= t1 + 1.0] or [r for _, r in rows]
+        inside = [r for ts, r in rows if t0 <= ts <= t1]
         if not inside:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         sm = [float(r[2]) for r in inside if r[2].replace(".", "").isdigit()]
@@ -217,6 +227,21 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm) if sm else None,
                 "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
                 "samples": len(inside)}
+
+
+def soak(step, flush, seconds: float, device):
+    """Run the same (flush, step) pair, untimed, for about ``seconds`` after
+    the timed region, so that the clock samples see the GPU under this load
+    even when the timed region itself is too short to sample."""
+    t_end = time.time() + seconds
+    n = 0
+    while time.time() < t_end:
+        for _ in range(20):
+            flush()
+            step()
+        n += 20
+        torch.cuda.synchronize(device)
+    return n
 
 
 # ------------------------------------------------------------ CPU oracle
@@ -361,6 +386,7 @@ def run_ours(args):
     if args.tuning:
         _native.set_tuning(**json.loads(args.tuning))
 
+    sampler = ClockSampler(local)
     spec = wl.SPECS[args.workload]
     w = wl.make_workload(spec, rank_seed(args.workload, rank), device=device)
     out, ws, err = harness.allocate(w, device)
@@ -380,7 +406,6 @@ def run_ours(args):
     if int(err.item()) != 0:
         raise SystemExit("device error word %d on warm-up" % int(err.item()))
 
-    sampler = ClockSampler(local)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     barrier(world)
@@ -395,8 +420,13 @@ def run_ours(args):
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(device)
     barrier(world)
+    soak_steps = soak(step, flush, args.clock_soak, device)
     t_wall1 = time.time()
     clocks = sampler.stop(t_wall0, t_wall1)
+    clocks["window"] = ("the timed region, then %d more flush+step pairs (untimed, %.1f s) "
+                        "of the same step" % (soak_steps, args.clock_soak))
+    if int(err.item()) != 0:
+        raise SystemExit("device error word %d after the timed steps" % int(err.item()))
     step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
     mean_ms = sum(step_ms) / len(step_ms)
     T = w.T
@@ -422,9 +452,13 @@ def run_ours(args):
         e2e_ms = max_over_ranks(e2e["ms"], world, device)
         e2e = {"value": rows_all / (e2e_ms / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": e2e["h2d"], "d2h_bytes_per_step": e2e["d2h"],
-               "ms_per_step": e2e_ms}
+               "ms_per_step": e2e_ms, "scope": E2E_SCOPE}
 
     graph = measure_graph(spec, args, device, run_step) if args.graph else None
+
+    workloads = None
+    if args.workloads and not args.early_exit and args.workload == "decode_b256":
+        workloads = measure_workloads(args, device, flush, rank)
 
     cpu = None
     if rank == 0 and world == 1 and args.cpu_baseline:
@@ -454,6 +488,8 @@ def run_ours(args):
         }
         if graph is not None:
             line["graph"] = graph
+        if workloads is not None:
+            line["workloads"] = workloads
         print(json.dumps(line))
     if world > 1:
         import torch.distributed as dist
@@ -478,6 +514,37 @@ def sampled_bytes(B, Kp, V, elt, rejected: int) -> dict:
     return parts
 
 
+def sampled_setup(device, rank, temperature):
+    """Inputs, outputs and the launch of one pe_verify_sampled call on the
+    large-batch decode shape."""
+    from speculative_decoding_pe_gb300 import _native
+    B, Kp, V = SAMPLED_SHAPE["B"], SAMPLED_SHAPE["Kp"], SAMPLED_SHAPE["V"]
+    s = wl.make_sampled_inputs(B, Kp, V, dtype=torch.bfloat16, seed=7100 + rank, device=device)
+    acc = torch.empty(B, dtype=torch.int32, device=device)
+    bon = torch.empty(B, dtype=torch.int32, device=device)
+    ws = torch.zeros(_native.workspace_bytes_sampled(B, Kp), dtype=torch.uint8, device=device)
+    err = _native.new_error_word(device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        _native.verify_sampled(s.target_logits, s.draft_logits, Kp, s.tokens, s.u_accept,
+                               temperature, 1234 + rank, acc, bon, ws, err, stream)
+    return s, acc, bon, ws, err, step
+
+
+def sampled_entry(args, device, flush, rank, steps, warm):
+    peak, _ = measured_peak()
+    B, Kp, V = SAMPLED_SHAPE["B"], SAMPLED_SHAPE["Kp"], SAMPLED_SHAPE["V"]
+    s, acc, bon, ws, err, step = sampled_setup(device, rank, args.temperature)
+    ms = time_steps(step, flush, torch.cuda.current_stream(device), steps, warm)
+    if int(err.item()) != 0 or int(ws.count_nonzero()) != 0:
+        raise SystemExit("sampled: device error word or workspace not zero")
+    rejected = int((acc < Kp).sum())
+    return _entry(ms, sampled_bytes(B, Kp, V, 2, rejected)["total"], peak,
+                  {"entry": "pe_verify_sampled", "rejecting_requests": rejected,
+                   "temperature": args.temperature})
+
+
 def run_sampled(args):
     """Time pe_verify_sampled (two launches per step) on the large-batch
     decode shape: B=256, K'=7, V=151936, bf16, temperature --temperature."""
@@ -487,20 +554,12 @@ def run_sampled(args):
     init_dist(world, "nccl")
     from speculative_decoding_pe_gb300 import _native
     _native.load()
+    sampler = ClockSampler(local)
     B, Kp, V = SAMPLED_SHAPE["B"], SAMPLED_SHAPE["Kp"], SAMPLED_SHAPE["V"]
-    seed = 7100 + rank
-    s = wl.make_sampled_inputs(B, Kp, V, dtype=torch.bfloat16, seed=seed, device=device)
-    acc = torch.empty(B, dtype=torch.int32, device=device)
-    bon = torch.empty(B, dtype=torch.int32, device=device)
-    ws = torch.zeros(_native.workspace_bytes_sampled(B, Kp), dtype=torch.uint8, device=device)
-    err = _native.new_error_word(device)
+    s, acc, bon, ws, err, step = sampled_setup(device, rank, args.temperature)
     flush = L2Flush(device, args.l2_flush)
     stream = torch.cuda.current_stream(device)
     T = args.temperature
-
-    def step():
-        _native.verify_sampled(s.target_logits, s.draft_logits, Kp, s.tokens, s.u_accept, T,
-                               1234 + rank, acc, bon, ws, err, stream)
 
     for _ in range(args.warmup):
         flush()
@@ -508,7 +567,6 @@ def run_sampled(args):
     torch.cuda.synchronize(device)
     if int(err.item()) != 0 or int(ws.count_nonzero()) != 0:
         raise SystemExit("device error word or workspace not zero after warm-up")
-    sampler = ClockSampler(local)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     barrier(world)
@@ -523,6 +581,7 @@ def run_sampled(args):
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(device)
     barrier(world)
+    soak(step, flush, args.clock_soak, device)
     t_wall1 = time.time()
     clocks = sampler.stop(t_wall0, t_wall1)
     step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
@@ -591,6 +650,35 @@ READOUT_METRIC = "greedy drafter readout rows/s"
 READOUT_SHAPE = {"B": 256, "K": 7, "V": 151936}  # the large-batch decode shape
 
 
+def readout_setup(device, rank):
+    """Drafter logits for B*K sampled rows, outputs, and the launch of one
+    pe_draft_readout call."""
+    from speculative_decoding_pe_gb300 import _native
+    B, K, V = READOUT_SHAPE["B"], READOUT_SHAPE["K"], READOUT_SHAPE["V"]
+    n = B * K
+    g = torch.Generator(device=device)
+    g.manual_seed(7300 + rank)
+    logits = (torch.randn(n, V, generator=g, device=device) * 2.0).to(torch.bfloat16)
+    out = torch.empty(n, dtype=torch.int32, device=device)
+    ws = _native.new_workspace(n, n, device)
+    err = _native.new_error_word(device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        _native.draft_readout(logits, out, ws, err, None, stream)
+    return logits, out, ws, err, step
+
+
+def readout_entry(args, device, flush, rank, steps, warm):
+    peak, _ = measured_peak()
+    logits, out, ws, err, step = readout_setup(device, rank)
+    ms = time_steps(step, flush, torch.cuda.current_stream(device), steps, warm)
+    if int(err.item()) != 0 or int(ws.count_nonzero()) != 0:
+        raise SystemExit("readout: device error word or workspace not zero")
+    n, V = logits.shape
+    return _entry(ms, n * V * 2 + 4 * n, peak, {"entry": "pe_draft_readout"})
+
+
 def run_readout(args):
     """Time pe_draft_readout (one launch) on the drafter's logits for the K
     sampled rows of each of B requests: argmax of B*K rows of V columns,
@@ -601,19 +689,12 @@ def run_readout(args):
     init_dist(world, "nccl")
     from speculative_decoding_pe_gb300 import _native
     _native.load()
+    sampler = ClockSampler(local)
     B, K, V = READOUT_SHAPE["B"], READOUT_SHAPE["K"], READOUT_SHAPE["V"]
     n = B * K
-    g = torch.Generator(device=device)
-    g.manual_seed(7300 + rank)
-    logits = (torch.randn(n, V, generator=g, device=device) * 2.0).to(torch.bfloat16)
-    out = torch.empty(n, dtype=torch.int32, device=device)
-    ws = _native.new_workspace(n, n, device)
-    err = _native.new_error_word(device)
+    logits, out, ws, err, step = readout_setup(device, rank)
     flush = L2Flush(device, args.l2_flush)
     stream = torch.cuda.current_stream(device)
-
-    def step():
-        _native.draft_readout(logits, out, ws, err, None, stream)
 
     for _ in range(args.warmup):
         flush()
@@ -621,7 +702,6 @@ def run_readout(args):
     torch.cuda.synchronize(device)
     if int(err.item()) != 0 or int(ws.count_nonzero()) != 0:
         raise SystemExit("device error word or workspace not zero after warm-up")
-    sampler = ClockSampler(local)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     barrier(world)
@@ -636,6 +716,7 @@ def run_readout(args):
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(device)
     barrier(world)
+    soak(step, flush, args.clock_soak, device)
     t_wall1 = time.time()
     clocks = sampler.stop(t_wall0, t_wall1)
     step_ms = [e0.elapsed_time(e1) for e0, e1 in ev]
@@ -684,11 +765,20 @@ def run_readout(args):
     return 0
 
 
+E2E_SCOPE = ("every input the step reads that changes from step to step (logits, target "
+             "hidden rows, input tokens and positions, block table, prompt offsets) copied "
+             "in from pinned host memory, and every output (accepted lengths, bonus tokens, "
+             "per-row argmax, offsets, tokens, positions, masks, hidden map, slot mapping, "
+             "sample_idx and X) copied back, every step; the embedding table and h_shared "
+             "stay resident")
+
+
 def measure_e2e(w, out, ws, err, packed, stream, device, args):
-    """The same step through the public API with inputs copied in from pinned
-    host memory and the per-request results copied back, every step."""
-    from speculative_decoding_pe_gb300 import _native
-    per_step = [w.logits, w.hidden, w.in_tokens, w.in_positions]
+    """The same step through the public API with its per-step inputs copied
+    in from pinned host memory and all of its outputs copied back, every
+    step (see E2E_SCOPE)."""
+    from speculative_decoding_pe_gb300 import _native, harness
+    per_step = [w.logits, w.hidden, w.in_tokens, w.in_positions, w.block_table]
     if w.in_offsets is not None:
         per_step.append(w.in_offsets)
     host = []
@@ -698,7 +788,7 @@ def measure_e2e(w, out, ws, err, packed, stream, device, args):
             host.append((base, base.cpu().pin_memory()))
         else:
             host.append((t, t.cpu().pin_memory()))
-    res_dev = [out.accepted_len, out.bonus_token]
+    res_dev = [getattr(out, k) for k in harness.OUTPUT_KEYS if getattr(out, k) is not None]
     res_host = [torch.empty_like(r, device="cpu").pin_memory() for r in res_dev]
     h2d = sum(h.numel() * h.element_size() for _, h in host)
     d2h = sum(r.numel() * r.element_size() for r in res_host)
@@ -723,6 +813,152 @@ def measure_e2e(w, out, ws, err, packed, stream, device, args):
     e1.record(stream)
     torch.cuda.synchronize(device)
     return {"ms": e0.elapsed_time(e1) / n, "h2d": h2d, "d2h": d2h}
+
+
+def time_steps(step, flush, stream, steps: int, warmup: int):
+    """Per-step milliseconds of ``step`` (CUDA events on ``stream``, the L2
+    flushed before each step, outside the events)."""
+    for _ in range(warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    for e0, e1 in ev:
+        flush()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+    torch.cuda.synchronize()
+    return [e0.elapsed_time(e1) for e0, e1 in ev]
+
+
+def time_graph(fn_list, stream, reps: int):
+    """Microseconds per captured call: ``fn_list`` (launches on the current
+    stream) captured once in a CUDA graph, replayed ``reps`` times."""
+    s = torch.cuda.Stream()
+    s.wait_stream(stream)
+    with torch.cuda.stream(s):
+        for f in fn_list:
+            f()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        for f in fn_list:
+            f()
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream()
+    e0.record(cur)
+    for _ in range(reps):
+        g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / (reps * len(fn_list))
+
+
+def _entry(step_ms, total_bytes, peak, extra=None):
+    mean = sum(step_ms) / len(step_ms)
+    achieved = total_bytes / (mean / 1e3) / 1e9
+    e = {"us_per_step": mean * 1e3, "median_us": statistics.median(step_ms) * 1e3,
+         "min_us": min(step_ms) * 1e3, "algorithmic_bytes": total_bytes,
+         "achieved_gbs": achieved, "roofline_frac": achieved / peak}
+    if extra:
+        e.update(extra)
+    return e
+
+
+def measure_workloads(args, device, flush, rank):
+    """Every other workload and every further entry point, each timed like
+    the headline (CUDA events per launch, L2 flushed between launches):
+    decode_b1 / decode_b64 / prefill_b8 / tiny through pe_step; decode_b1
+    also inside a CUDA graph, against the latency floor (an empty launch of
+    the step's grid, and the same plus one dependent global round trip);
+    early exit at B=256 (against the bytes of the rows it needs); the
+    drafter readout; rejection sampling; the no-allocation step."""
+    from speculative_decoding_pe_gb300 import _native, harness
+    peak, _ = measured_peak()
+    stream = torch.cuda.current_stream(device)
+    steps, warm = args.workload_steps, max(3, args.warmup)
+    res = {}
+    for name in ("decode_b1", "decode_b64", "prefill_b8", "tiny"):
+        spec = wl.SPECS[name]
+        w = wl.make_workload(spec, rank_seed(name, rank), device=device)
+        out, ws, err = harness.allocate(w, device)
+        packed = harness.pack(w, out, ws, err)
+        ms = time_steps(lambda: _native.step_packed(packed, stream), flush, stream, steps, warm)
+        torch.cuda.synchronize()
+        if int(err.item()) != 0:
+            raise SystemExit("device error word %d (%s)" % (int(err.item()), name))
+        b = algorithmic_bytes(spec, w.R)["total"]
+        res[name] = _entry(ms, b, peak, {"rows_per_s": w.T / (sum(ms) / len(ms) / 1e3),
+                                         "entry": "pe_step"})
+        if name == "decode_b1":
+            # the same step captured 16 times (16 input sets) in one graph
+            ws_list = [wl.make_workload(spec, 9100 + i, device=device) for i in range(16)]
+            wsp = _native.new_workspace(spec.B * (spec.Kp + 1), spec.B, device)
+            bufs = [harness.allocate(x, device) for x in ws_list]
+            packs = [harness.pack(x, o, wsp, e) for x, (o, _, e) in zip(ws_list, bufs)]
+            res[name]["graph_us_per_step"] = time_graph(
+                [lambda a=a: _native.step_packed(a) for a in packs], stream, 50)
+            grid = torch.cuda.get_device_properties(device).multi_processor_count * \
+                _native.get_tuning()["ctas_per_sm"]
+            chain = torch.zeros(1, dtype=torch.int32, device=device)
+            sink = torch.zeros(1, dtype=torch.int32, device=device)
+            empty = time_steps(lambda: _native.latency_floor(grid, 0, stream=stream), flush,
+                               stream, steps, warm)
+            hop = time_steps(lambda: _native.latency_floor(grid, 1, chain, sink, stream),
+                             flush, stream, steps, warm)
+            res[name]["floor"] = {
+                "grid_ctas": grid,
+                "empty_launch_us": statistics.median(empty) * 1e3,
+                "empty_plus_one_round_trip_us": statistics.median(hop) * 1e3,
+                "empty_launch_graph_us": time_graph(
+                    [lambda: _native.latency_floor(grid, 0)] * 16, stream, 50),
+                "empty_plus_one_round_trip_graph_us": time_graph(
+                    [lambda: _native.latency_floor(grid, 1, chain, sink)] * 16, stream, 50),
+                "note": "launched: the L2 flushed before each launch, so the round trip "
+                        "goes to HBM; in the graph it hits L2"}
+            del ws_list, bufs, packs
+        del w, out, ws, err, packed
+        torch.cuda.empty_cache()
+    # early exit at B=256: rows 0..a_b of each request are what it must read
+    spec = wl.SPECS["decode_b256"]
+    w = wl.make_workload(spec, rank_seed("decode_b256", rank), device=device)
+    out, ws, err = harness.allocate(w, device)
+    packed = harness.pack(w, out, ws, err)
+    ms = time_steps(lambda: _native.step_early_exit_packed(packed, stream), flush, stream,
+                    steps, warm)
+    needed = int((w.planted_accept.long() + 1).sum())
+    res["early_exit_decode_b256"] = _entry(
+        ms, algorithmic_bytes(spec, w.R, needed)["total"], peak,
+        {"entry": "pe_step_early_exit", "logits_rows_needed": needed,
+         "logits_rows": w.B * (w.Kp + 1)})
+    # the no-allocation step (its scratch cleared by a memset each call)
+    lib = _native.load()
+    import ctypes
+    nb = algorithmic_bytes(spec, w.R)["total"]
+    def noalloc_call(args_):
+        if lib.pe_step_noalloc(ctypes.byref(args_), ctypes.c_void_p(stream.cuda_stream)) != 0:
+            raise SystemExit("pe_step_noalloc rejected its arguments")
+
+    ms = time_steps(lambda: noalloc_call(packed), flush, stream, steps, warm)
+    res["noalloc_decode_b256"] = _entry(ms, nb, peak, {"entry": "pe_step_noalloc"})
+    del w, out, ws, err, packed
+    w1 = wl.make_workload("decode_b1", rank_seed("decode_b1", rank), device=device)
+    out1, ws1, err1 = harness.allocate(w1, device)
+    p1 = harness.pack(w1, out1, ws1, err1)
+    ms = time_steps(lambda: noalloc_call(p1), flush, stream, steps, warm)
+    res["noalloc_decode_b1"] = _entry(ms, algorithmic_bytes(w1.spec, w1.R)["total"], peak,
+                                      {"entry": "pe_step_noalloc"})
+    del w1, out1, ws1, err1, p1
+    torch.cuda.empty_cache()
+    # drafter readout and rejection sampling (their own bench modes)
+    res["readout_decode_b256"] = readout_entry(args, device, flush, rank, steps, warm)
+    res["sampled_decode_b256"] = sampled_entry(args, device, flush, rank, steps, warm)
+    return res
 
 
 def measure_graph(spec, args, device, run_step):
@@ -800,6 +1036,13 @@ def main(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-e2e", dest="e2e", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--no-workloads", dest="workloads", action="store_false",
+                    help="skip the extra per-workload entries of the default line")
+    ap.add_argument("--workload-steps", type=int, default=50,
+                    help="timed launches per extra workload entry")
+    ap.add_argument("--clock-soak", type=float, default=1.0,
+                    help="seconds of untimed steps after the timed region, sampled "
+                         "for the clocks record")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         raise SystemExit("--warmup must be at least 3")

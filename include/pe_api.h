@@ -72,9 +72,10 @@ typedef enum pe_dtype { PE_F32 = 0, PE_BF16 = 1 } pe_dtype;
 #define PE_ERR_OFFSETS 8u     /* in_offsets invalid: nothing is written     */
 #define PE_ERR_MAP_RANGE 16u  /* hidden_map entry outside [0,T): skipped    */
 #define PE_ERR_ROW_RANGE 64u  /* readout row index outside [0,rows): -1     */
-#define PE_ERR_TIMEOUT 32u    /* a bounded wait gave up (the pipelined
-                                 step's ring, the sampled stats merge);
-                                 outputs incomplete; never expected        */
+#define PE_ERR_TIMEOUT 32u    /* a bounded wait gave up (a bulk-copy tile
+                                 waiting for its own loads, the sampled
+                                 stats merge); outputs incomplete; never
+                                 expected with a zeroed workspace          */
 /* Raised only by the checked build (libpe_checked.so: the same entry points
  * compiled with PE_CHECKED, for debugging; slower).  Neither traps. */
 #define PE_ERR_NAN 128u       /* a logits row read by the greedy argmax
@@ -84,6 +85,20 @@ typedef enum pe_dtype { PE_F32 = 0, PE_BF16 = 1 } pe_dtype;
 #define PE_ERR_INTERNAL 256u  /* an internal index invariant of the fused
                                  step failed; the access was skipped (never
                                  expected: a library bug)                  */
+/* Raised by every build. */
+#define PE_ERR_WORKSPACE 512u /* a workspace counter or hand-off word held a
+                                 value outside its legal range: the
+                                 workspace was not zero when the call
+                                 started (never zero-filled, shared by
+                                 calls that overlap on the GPU, or left
+                                 dirty by an earlier call that raised
+                                 PE_ERR_TIMEOUT or PE_ERR_WORKSPACE).  The
+                                 call skipped the work the bad value
+                                 governs: outputs are incomplete, and the
+                                 workspace must be zero-filled again before
+                                 its next use.  Detection is by range: a
+                                 corruption that keeps every value inside
+                                 its legal range goes unseen.              */
 
 /* Limits checked on the host. */
 #define PE_MAX_KP 255 /* previous draft depth K'  */
@@ -93,8 +108,11 @@ typedef enum pe_dtype { PE_F32 = 0, PE_BF16 = 1 } pe_dtype;
  * logits_rows = B = n), pe_step and pe_step_early_exit need for a batch with
  * `logits_rows` = B*(Kp+1) logits rows and B requests.  The caller
  * allocates it once, zero-filled, and may reuse it for every later call of
- * any size up to those; each call leaves it zeroed again on completion.
- * Calls that may run concurrently need separate workspaces. */
+ * any size up to those; each call leaves it zeroed again on completion,
+ * unless it raised PE_ERR_TIMEOUT or PE_ERR_WORKSPACE: after either bit the
+ * caller zero-fills the workspace again (a caller that does not tell the
+ * bits apart may simply do so after any bit).  Calls that may run
+ * concurrently need separate workspaces. */
 size_t pe_workspace_bytes(int32_t logits_rows, int32_t B);
 
 /* Greedy verification [P1 quick-read: acceptance length].
@@ -107,7 +125,7 @@ size_t pe_workspace_bytes(int32_t logits_rows, int32_t B);
  *  bonus_token [B] out: argmax of row a_b (the target's own next token).
  *  target_argmax [B*(Kp+1)] out, or NULL: every row's argmax.
  *  workspace   pe_workspace_bytes(B*(Kp+1), B) bytes, zeroed (see above).
- *  err         device error word (no bits are defined for this call).
+ *  err         device error word (PE_ERR_WORKSPACE only).
  * B == 0 enqueues nothing. */
 int pe_verify_greedy(const void* logits, int dtype, int64_t row_stride,
                      int32_t B, int32_t Kp, int32_t V, const int32_t* in_tokens,
@@ -134,8 +152,9 @@ int pe_draft_readout(const void* logits, int dtype, int64_t row_stride,
                      uint32_t* err, void* stream);
 
 /* Bytes of scratch that pe_verify_sampled needs for B requests of depth Kp
- * (any V).  Allocated once, zero-filled; every call leaves it zeroed again,
- * so it serves every later call with B and Kp up to those. */
+ * (any V).  Allocated once, zero-filled; every call leaves it zeroed again
+ * (except after PE_ERR_TIMEOUT or PE_ERR_WORKSPACE, as above), so it serves
+ * every later call with B and Kp up to those. */
 size_t pe_workspace_bytes_sampled(int32_t B, int32_t Kp);
 
 /* Rejection-sampling verification [P3 §1.2], read as the acceptance rule of
@@ -163,7 +182,8 @@ size_t pe_workspace_bytes_sampled(int32_t B, int32_t Kp);
  *  temperature   > 0 (PE_EINVAL otherwise); logits must be finite.
  *  workspace     pe_workspace_bytes_sampled(B, Kp) bytes, zeroed.
  *  err           device error word: PE_ERR_TIMEOUT when a bounded wait of
- *                the statistics merge gave up (never expected).
+ *                the statistics merge gave up (never expected with a zeroed
+ *                workspace); PE_ERR_WORKSPACE as above.
  * Arithmetic is fp32 in the log2 domain (the hardware's approximate ex2 and
  * lg2 instructions; near U = 1 the noise uses a short series of
  * -log2(1 - t) instead): accept decisions and draws agree with
@@ -303,7 +323,10 @@ int pe_step_early_exit(const pe_step_args* args /* host */, void* stream);
  * the library, held by every GPU that loads it until the process exits.
  *  - The first call on a device looks up the array's device address (and
  *    may load the library's GPU code there): make that first call before
- *    any stream capture.
+ *    any stream capture.  The address is kept for the life of the process;
+ *    a program that resets a device (cudaDeviceReset) must not call this
+ *    entry point on that device afterwards (the kept address would no
+ *    longer be the array's).
  *  - Each call enqueues a memset clearing the scratch it needs, then the
  *    step; if pe_step then rejects the arguments, the memset has still been
  *    enqueued (it touches only the library's own array).
@@ -321,7 +344,14 @@ typedef struct pe_tuning {
   int32_t ctas_per_sm;     /* resident CTAs per SM for the persistent grid */
   int32_t chunk_batches;   /* max 32 KiB load batches per argmax unit      */
   int32_t rows_per_unit;   /* X rows per copy unit                         */
-  int32_t variant;         /* 1: register streaming, 2: bulk-copy pipeline */
+  int32_t variant;         /* how copy tiles move X's half rows (the argmax
+                              streams through registers either way):
+                              1: 16-byte loads and stores through registers
+                              (default); 2: bulk asynchronous copies
+                              (cp.async.bulk) global -> shared -> global,
+                              one thread issuing them, with as many rows
+                              per tile as a 48 KiB staging buffer holds
+                              (register copies when not even one fits) */
   int32_t queue_order;     /* 2: argmax chunks first, every copy tile after
                               (default: the tiles fill the drain, and a
                               request's last verified-row tile, not its
@@ -339,6 +369,18 @@ typedef struct pe_tuning {
 } pe_tuning;
 int pe_get_tuning(pe_tuning* out /* host */);
 int pe_set_tuning(const pe_tuning* in /* host */);
+
+/* Launch-latency reference (no counterpart on the pages: a measuring aid).
+ * Launches `ctas` CTAs of 256 threads on `stream` that do no work, except
+ * that thread 0 of CTA 0 follows `hops` dependent 4-byte loads through
+ * `chain` [n] int32 (entry i holds the index of the next entry; an index
+ * outside [0, n) continues from entry 0) and stores the last index to
+ * *out.  hops = 0: an empty launch (chain and out may be NULL).  At small
+ * batch the fused step is a chain of dependent round trips, and this is the
+ * floor it is measured against: an empty launch of the step's grid, plus
+ * one round trip to global memory. */
+int pe_latency_floor(int32_t ctas, int32_t hops, const int32_t* chain, int32_t n,
+                     int32_t* out, void* stream);
 
 /* Human-readable name of a pe_status value. */
 const char* pe_status_str(int status);

@@ -31,6 +31,7 @@ ERR_TIMEOUT = 32
 ERR_ROW_RANGE = 64
 ERR_NAN = 128
 ERR_INTERNAL = 256
+ERR_WORKSPACE = 512
 MAX_KP, MAX_K = 255, 256
 
 # every function the C header declares
@@ -39,7 +40,7 @@ EXPORTS = ("pe_workspace_bytes", "pe_verify_greedy", "pe_draft_readout",
            "pe_build_draft_batch",
            "pe_assemble_draft_inputs", "pe_step", "pe_step_early_exit", "pe_step_noalloc",
            "pe_get_tuning",
-           "pe_set_tuning", "pe_status_str")
+           "pe_set_tuning", "pe_latency_floor", "pe_status_str")
 
 
 class PEError(RuntimeError):
@@ -130,6 +131,8 @@ def _open(path: str):
     lib.pe_step_noalloc.restype = ctypes.c_int
     lib.pe_get_tuning.argtypes = [ctypes.POINTER(Tuning)]
     lib.pe_set_tuning.argtypes = [ctypes.POINTER(Tuning)]
+    lib.pe_latency_floor.argtypes = [i32, i32, P, i32, P, P]
+    lib.pe_latency_floor.restype = ctypes.c_int
     lib.pe_status_str.argtypes = [ctypes.c_int]
     lib.pe_status_str.restype = ctypes.c_char_p
     for f in ("pe_verify_greedy", "pe_build_draft_batch", "pe_assemble_draft_inputs",
@@ -407,6 +410,16 @@ def step(**kw):
     make_step_args for the arguments and an optional ``stream``."""
     stream = kw.pop("stream", None)
     step_packed(make_step_args(**kw), stream)
+
+
+def latency_floor(ctas: int, hops: int = 0, chain=None, out=None, stream=None):
+    """An empty launch of ``ctas`` CTAs, plus ``hops`` dependent loads through
+    ``chain`` (int32, entry i = index of the next) ending in ``out[0]``."""
+    lib = load()
+    n = chain.numel() if chain is not None else 0
+    rc = lib.pe_latency_floor(ctas, hops, _dev(chain, "chain", torch.int32), n,
+                              _dev(out, "out", torch.int32, 1), _stream(stream))
+    _check(lib, rc, "pe_latency_floor")
 
 
 def get_tuning() -> dict:

@@ -44,6 +44,13 @@ __device__ __forceinline__ void fence_acq_rel() {
   asm volatile("fence.acq_rel.gpu;" ::: "memory");
 }
 
+// Global time in nanoseconds (bounds the few waits).
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
 // Total order on non-NaN floats as unsigned integers, with -0.0 == +0.0.
 __device__ __forceinline__ uint32_t ordered_bits(float f) {
   uint32_t b = __float_as_uint(f);

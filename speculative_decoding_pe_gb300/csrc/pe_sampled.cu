@@ -354,7 +354,7 @@ __device__ __forceinline__ void fold_chunk(const SampledParams& p, const char* r
 // never NaN (it starts finite and only takes larger values), and its bits
 // are stored XOR a quiet-NaN pattern.
 constexpr uint32_t kPartialMark = 0x7fc00000u;
-constexpr int kPollLimit = 1 << 20;  // loads of a slot before giving up
+constexpr unsigned long long kPollLimitNs = 2000000ull;  // 2 ms per slot before giving up
 
 __device__ __forceinline__ unsigned long long pack_partial(float2 t) {
   return ((unsigned long long)(__float_as_uint(t.x) ^ kPartialMark) << 32) | __float_as_uint(t.y);
@@ -390,9 +390,16 @@ __device__ __forceinline__ void decide(const SampledParams& p, int b) {
   p.accepted_len[b] = a;
   if (a < p.Kp) {  // a rejection: list the request for the residual pass
     p.acc[b] = a;  // (the residual draw clears it)
-    p.rlist[atomicAdd(p.sched + 4, 1u)] = b;
+    const unsigned at = atomicAdd(p.sched + 4, 1u);
+    if (at < (unsigned)p.B)
+      p.rlist[at] = b;
+    else  // the list count did not start at zero
+      atomicOr(p.err, PE_ERR_WORKSPACE);
   }
   const unsigned long long gk = atomicExch(p.gkey + b, 0ull);
+  // the bonus row's draw names a column of the row (a finite row always
+  // yields one)
+  if (gk == 0ull || key_col(gk) >= (uint32_t)p.V) atomicOr(p.err, PE_ERR_WORKSPACE);
   if (a == p.Kp) p.bonus_token[b] = (int)key_col(gk);  // else the residual pass draws
   for (int j = 0; j <= p.Kp; ++j) {
     const int vt = b * (p.Kp + 1) + j;
@@ -454,7 +461,9 @@ __device__ __forceinline__ void stats_finish(const SampledParams& p, int vr, int
       atomicMax(p.gkey + b, gk);
       fence_acq_rel();  // release
     }
-    last = atomicAdd(p.rcount + vr, 1u) == (unsigned)(p.C - 1);
+    const unsigned done = atomicAdd(p.rcount + vr, 1u);
+    if (done >= (unsigned)p.C) atomicOr(p.err, PE_ERR_WORKSPACE);  // did not start at zero
+    last = done == (unsigned)(p.C - 1);
     if (last) fence_acq_rel();  // acquire: the bonus row's key
   }
   if (!__shfl_sync(0xffffffffu, last, 0)) return;
@@ -463,7 +472,10 @@ __device__ __forceinline__ void stats_finish(const SampledParams& p, int vr, int
   for (int cc = lane; cc < p.C; cc += 32) {
     unsigned long long* slot = p.partial + vr * kMaxChunksSampled + cc;
     unsigned long long w = ld_relaxed(slot);
-    for (int it = 0; w == 0ull && it < kPollLimit; ++it) w = ld_relaxed(slot);
+    if (w == 0ull) {
+      const unsigned long long t0 = global_ns();
+      while (w == 0ull && global_ns() - t0 < kPollLimitNs) w = ld_relaxed(slot);
+    }
     if (w == 0ull)
       atomicOr(p.err, PE_ERR_TIMEOUT);  // never expected: the chunk was counted
     else
@@ -480,7 +492,9 @@ __device__ __forceinline__ void stats_finish(const SampledParams& p, int vr, int
       p.prob[vr] = (x >= 0 && x < p.V) ? ex2(E::at(rowp, x) * p.c2 - L) : -1.f;
     }
     fence_acq_rel();  // release
-    if (atomicAdd(p.qcount + b, 1u) == (unsigned)(2 * p.Kp)) {  // all 2Kp+1 rows
+    const unsigned rows_done = atomicAdd(p.qcount + b, 1u);
+    if (rows_done > (unsigned)(2 * p.Kp)) atomicOr(p.err, PE_ERR_WORKSPACE);
+    if (rows_done == (unsigned)(2 * p.Kp)) {  // all 2Kp+1 rows
       p.qcount[b] = 0u;
       fence_acq_rel();  // acquire: every row's probability
       decide(p, b);
@@ -522,14 +536,18 @@ __device__ __forceinline__ uint32_t* stats_counter(const SampledParams& p, int i
 }
 
 // Next unit for this warp (lane 0), or n_units once every counter ran out.
+// A counter hands out its n_i units and then one failing claim per warp, so
+// a value above n_i + warps - 1 means it did not start at zero.
 __device__ __forceinline__ int stats_next(const SampledParams& p, int n_units, int& ci,
                                           int& ndone) {
   while (ndone < kStatsCounters) {
     const int n_i = (n_units - ci + kStatsCounters - 1) / kStatsCounters;
     uint32_t* ctr = stats_counter(p, ci);
     const unsigned v = atomicAdd(ctr, 1u);
-    if (v == (unsigned)n_i + gridDim.x * kWarps - 1u) atomicExch(ctr, 0u);
-    if ((int)v < n_i) return ci + (int)v * kStatsCounters;
+    const unsigned last = (unsigned)n_i + gridDim.x * kWarps - 1u;
+    if (v == last) atomicExch(ctr, 0u);
+    if (v > last) atomicOr(p.err, PE_ERR_WORKSPACE);
+    if (v < (unsigned)n_i) return ci + (int)v * kStatsCounters;
     ++ndone;
     ci = ci + 1 == kStatsCounters ? 0 : ci + 1;
   }
@@ -564,8 +582,12 @@ __device__ __forceinline__ void residual_unit(const SampledParams& p, int u, int
   using E = Vec<DT>;
   const int b = u / p.C2;
   const int c = u - b * p.C2;
-  const int a = __ldcg(p.acc + b);
-  const bool draw = a < p.Kp;  // else the stats pass drew the bonus already
+  int a = __ldcg(p.acc + b);
+  if (a < 0 || a >= p.Kp) {  // a listed request has a rejection at a < K'
+    if (c == 0) atomicOr(p.err, PE_ERR_WORKSPACE);
+    a = p.Kp;  // nothing to draw
+  }
+  const bool draw = a < p.Kp;
   const int vt = b * (p.Kp + 1) + a;
   const int vd = p.Rt + b * p.Kp + a;
   Best best;
@@ -631,7 +653,9 @@ __device__ __forceinline__ void residual_unit(const SampledParams& p, int u, int
   if (lane == 0) {
     if (draw) atomicMax(p.rkey + b, k);
     fence_acq_rel();  // release
-    last = atomicAdd(p.dcount + b, 1u) == (unsigned)(p.C2 - 1);  // every unit of b is done
+    const unsigned done = atomicAdd(p.dcount + b, 1u);
+    if (done >= (unsigned)p.C2) atomicOr(p.err, PE_ERR_WORKSPACE);  // did not start at zero
+    last = done == (unsigned)(p.C2 - 1);  // every unit of b is done
     if (last) fence_acq_rel();  // acquire
   }
   if (!__shfl_sync(0xffffffffu, last, 0)) return;
@@ -642,6 +666,7 @@ __device__ __forceinline__ void residual_unit(const SampledParams& p, int u, int
     p.acc[b] = 0;
     if (draw) {
       const unsigned long long r = atomicExch(p.rkey + b, 0ull);
+      if (r && key_col(r) >= (uint32_t)p.V) atomicOr(p.err, PE_ERR_WORKSPACE);
       if (r) p.bonus_token[b] = (int)key_col(r);
       else fallback = 1;
       p.lse[vt] = 0.f;
@@ -668,17 +693,31 @@ __device__ __forceinline__ void residual_unit(const SampledParams& p, int u, int
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 4) sampled_residual_kernel(const SampledParams p) {
   const int lane = threadIdx.x & 31;
-  const int n_units = (int)__ldcg(p.sched + 4) * p.C2;
+  const int warp = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  // at most B requests are listed; more means the count did not start at
+  // zero (every warp reads the same value, one warp reports it)
+  unsigned listed = __ldcg(p.sched + 4);
+  if (listed > (unsigned)p.B) {
+    if (warp == 0 && lane == 0) atomicOr(p.err, PE_ERR_WORKSPACE);
+    listed = (unsigned)p.B;
+  }
+  const int n_units = (int)listed * p.C2;
   const int nw = gridDim.x * kWarps;
-  for (int u = blockIdx.x * kWarps + (threadIdx.x >> 5); u < n_units; u += nw) {
+  for (int u = warp; u < n_units; u += nw) {
     const int k = u / p.C2;
-    residual_unit<DT>(p, __ldcg(p.rlist + k) * p.C2 + (u - k * p.C2), lane);
+    const int b = __ldcg(p.rlist + k);
+    if (b < 0 || b >= p.B) {  // an entry this call did not write
+      if (lane == 0 && u == k * p.C2) atomicOr(p.err, PE_ERR_WORKSPACE);
+      continue;
+    }
+    residual_unit<DT>(p, b * p.C2 + (u - k * p.C2), lane);
   }
   if (lane == 0) {
     fence_acq_rel();  // release
-    if (atomicAdd(p.sched + 3, 1u) == gridDim.x * kWarps - 1) {  // every other warp has left
+    const unsigned left = atomicAdd(p.sched + 3, 1u);
+    if (left > gridDim.x * kWarps - 1u) atomicOr(p.err, PE_ERR_WORKSPACE);
+    if (left == gridDim.x * kWarps - 1u) {  // every other warp has left
       fence_acq_rel();  // acquire: their reads of the list come first
-      const unsigned listed = p.sched[4];
       for (unsigned k = 0; k < listed; ++k) p.rlist[k] = 0;
       atomicExch(p.sched + 3, 0u);
       atomicExch(p.sched + 4, 0u);

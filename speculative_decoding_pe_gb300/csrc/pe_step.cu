@@ -14,9 +14,7 @@
 //    vLLM" -- quick-read section: Input_1 = emb(new) (+) h_context,
 //    Input_i = emb(mask) (+) h_shared for 2 <= i <= K; acceptance length.
 //
-// Design (one launch, no grid-wide barrier; the register-streaming kernel
-// has no spin-wait, the pipelined variant's waits on its own bulk-copy ring
-// are bounded):
+// Design (one launch, no grid-wide barrier, no CTA ever waits for another):
 //  * A persistent grid pulls work units from a counter in the workspace.
 //    Units [0, n_arg) are argmax chunks (row r, chunk c) of the logits, in
 //    row order; units [n_arg, n_units) copy tiles of X rows, first those of
@@ -40,6 +38,17 @@
 //    writer.
 //  * Each CTA takes one index past the end of the queue and leaves; the
 //    claim that returns the last index resets the counter for the next call.
+//  * Copy tiles move their half rows through registers (16-byte loads and
+//    stores), or, with pe_tuning.variant = 2, through shared memory with
+//    bulk asynchronous copies (one thread issues a load per half row into a
+//    staging buffer, waits on the CTA's barrier, and issues the bulk stores
+//    into X).
+//  * Workspace words are checked against their legal ranges as they are
+//    used (a unit index past the queue, a count past its total, a hand-off
+//    word or state word with bits no call sets, a row key whose column is
+//    outside the vocabulary); a bad value raises PE_ERR_WORKSPACE and the
+//    work it governs is skipped, so a dirty workspace never sends an access
+//    out of bounds.
 //  * Early exit reads a request's rows in order and skips the rows after a
 //    known mismatch (step_kernel_early); with a small logits footprint the
 //    host serves it with the full read instead, the epilogue writing -1 to
@@ -50,19 +59,11 @@
 
 namespace pe {
 
-// Barrier over the threads that do a unit's work: the whole CTA in the
-// register-streaming kernel, the eight consumer warps in the pipelined one.
-struct SyncAll {
-  __device__ static __forceinline__ void sync() { __syncthreads(); }
-};
-struct SyncConsumers {
-  __device__ static __forceinline__ void sync() { named_sync<kThreads>(); }
-};
-
 struct StepParams {
   int B, Kp, K, V, H, R, T, mask_id, bt_width, block_size;
   int full;               // 1: rebuild + assemble too; 0: verification only
   int nvh;                // 16-byte vectors per half row of X
+  int bulk_rows;          // bulk-copy tiles: X rows the staging buffer holds
   long long row_bytes;    // logits row stride in bytes
   int nvec, tail;         // whole 16-byte vectors per logits row, leftover elements
   int chunk_vecs, C, Rl;  // argmax chunking: vectors per chunk, chunks per row, rows
@@ -106,10 +107,10 @@ enum SegMode { kSkip = 0, kCopy = 1, kZero = 2 };
 
 struct SharedState {
   unsigned long long red[kWarps];
+  uint64_t bar;                // bulk-copy tiles: completion of the tile's loads
   int unit;
   int last;
   int first;
-  int verdict[2];
   int amax[PE_MAX_KP + 1];
   int tok[PE_MAX_KP + 1];
   int pos[PE_MAX_KP + 1];
@@ -129,6 +130,20 @@ struct SharedState {
 // (bit 16), accepted length (bits 17-24), bonus token (bits 32-63).
 constexpr unsigned long long kXferCount = 0xffffull;
 constexpr unsigned long long kXferVerdict = 1ull << 16;
+
+// A hand-off word as a legal call can leave it for the side that updates it
+// next: the tiles' count below K'+1 (a tile adding its rows) or at most K'+1
+// (the verdict), bits 25-31 clear, and either no verdict yet (nothing above
+// the count) or, for a tile, a verdict with a <= K'.  Anything else means the
+// workspace was not zero when the call started.
+__device__ __forceinline__ bool xfer_legal(unsigned long long w, int Kp, bool tile_side) {
+  const unsigned long long cnt = w & kXferCount;
+  if (tile_side ? cnt >= (unsigned long long)(Kp + 1) : cnt > (unsigned long long)(Kp + 1))
+    return false;
+  if (w & 0xfe000000ull) return false;
+  if (!(w & kXferVerdict)) return (w >> 17) == 0ull;
+  return tile_side && ((w >> 17) & 0xffull) <= (unsigned long long)Kp;
+}
 
 // Unit handed out at position q of the queue.  vfirst: the copy tiles of
 // the verified rows first, then the argmax chunks, then the other copy tiles
@@ -222,7 +237,7 @@ struct Elem<PE_F32> {
 // EARLY: the accepted length `a_known` is already settled (early-exit step);
 // rows 0..a_known are read from the completed-row results and later rows,
 // which may never have been read, report -1.
-template <class S, bool EARLY = false>
+template <bool EARLY = false>
 __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedState& sh,
                                                  int b, int a_known = -1) {
   const int tid = threadIdx.x;
@@ -236,7 +251,11 @@ __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedStat
       sh.amax[tid] = tid <= a_known ? __ldcg(p.amax_ws + (long long)b * nr + tid) : -1;
     } else {
       const unsigned long long k = atomicExch(p.keys + (long long)b * nr + tid, 0ull);
-      sh.amax[tid] = (int)key_col(k);
+      const uint32_t col = key_col(k);
+      // a merged key names a column of the row (0: a readout row outside the
+      // logits, which holds no element)
+      if (k != 0ull && col >= (uint32_t)p.V) atomicOr(p.err, PE_ERR_WORKSPACE);
+      sh.amax[tid] = (int)col;
     }
     if (tid < Kp) sh.tok[tid] = __ldg(p.in_tokens + io + vb + tid + 1);  // draft d_{tid+1}
     if (p.full) sh.pos[tid] = __ldg(p.in_positions + io + vb + tid);
@@ -245,10 +264,10 @@ __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedStat
     sh.first = EARLY ? a_known : Kp;
     if (!EARLY) atomicExch(p.count + b, 0u);
   }
-  S::sync();
+  __syncthreads();
   // accepted length: first draft that differs from the target's choice
   if (!EARLY && tid < Kp && sh.amax[tid] != sh.tok[tid]) atomicMin(&sh.first, tid);
-  S::sync();
+  __syncthreads();
   const int a = sh.first;
   if (p.target_argmax && tid < nr)
     p.target_argmax[(long long)b * nr + tid] = p.mask_unread && tid > a ? -1 : sh.amax[tid];
@@ -326,14 +345,16 @@ __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedStat
     }
   }
   if (tid == 0) {
-    const bool mine = (old & kXferCount) == (unsigned long long)nr;
+    const bool legal = xfer_legal(old, Kp, false);
+    if (!legal) atomicOr(p.err, PE_ERR_WORKSPACE);
+    const bool mine = legal && (old & kXferCount) == (unsigned long long)nr;
     if (mine) {
       atomicExch(p.xfer + b, 0ull);  // both sides are done: clear for the next call
       fence_acq_rel();  // acquire: the tiles' writes of the row come before ours
     }
     sh.xwrite = mine ? 1 : 0;
   }
-  S::sync();
+  __syncthreads();
   if (sh.xwrite && PE_INVARIANT(p.err, oo + s >= 0 && oo + s < p.T)) {
     uint4* dst = p.X + (long long)(oo + s) * 2 * p.nvh;
     if (tid < p.nvh) dst[tid] = x1;
@@ -344,7 +365,7 @@ __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedStat
 }
 
 // ------------------------------------------------------------- argmax chunk
-template <class S, int DT>
+template <int DT>
 __device__ __forceinline__ void finish_argmax_unit(const StepParams& p, SharedState& sh, int r,
                                                    int c, const char* rowp,
                                                    unsigned long long key);
@@ -415,13 +436,13 @@ __device__ __forceinline__ void argmax_unit(const StepParams& p, SharedState& sh
   if (!rowp && c == 0 && tid == 0) atomicOr(p.err, PE_ERR_ROW_RANGE);
   const unsigned long long key =
       thread_key<DT>(reinterpret_cast<const uint4*>(rowp), v_lo, v_hi, p.err);
-  finish_argmax_unit<SyncAll, DT>(p, sh, r, c, rowp, key);
+  finish_argmax_unit<DT>(p, sh, r, c, rowp, key);
 }
 
 // End of an argmax unit: fold in the leftover elements, reduce the threads'
 // keys, merge into the row's key, and run the request's epilogue in the CTA
 // whose unit completes the request.
-template <class S, int DT>
+template <int DT>
 __device__ __forceinline__ void finish_argmax_unit(const StepParams& p, SharedState& sh, int r,
                                                    int c, const char* rowp,
                                                    unsigned long long key) {
@@ -454,7 +475,7 @@ __device__ __forceinline__ void finish_argmax_unit(const StepParams& p, SharedSt
 
   key = warp_max_key(key);
   if ((tid & 31) == 0) sh.red[tid >> 5] = key;
-  S::sync();
+  __syncthreads();
   if (tid < 32) {
     unsigned long long k = tid < kWarps ? sh.red[tid] : 0ull;
     k = warp_max_key(k);
@@ -462,15 +483,17 @@ __device__ __forceinline__ void finish_argmax_unit(const StepParams& p, SharedSt
       atomicMax(p.keys + r, k);
       fence_acq_rel();  // release
       const int b = r / (p.Kp + 1);
+      const unsigned total = (unsigned)((p.Kp + 1) * p.C);
       const unsigned done = atomicAdd(p.count + b, 1u);
-      const bool last = done == (unsigned)((p.Kp + 1) * p.C - 1);
+      if (done >= total) atomicOr(p.err, PE_ERR_WORKSPACE);  // did not start at zero
+      const bool last = done == total - 1u;
       if (last) fence_acq_rel();  // acquire: every chunk of the request is in
       sh.last = last ? b : -1;
     }
   }
-  S::sync();
+  __syncthreads();
   const int last = sh.last;
-  if (last >= 0) request_epilogue<S>(p, sh, last);
+  if (last >= 0) request_epilogue(p, sh, last);
 }
 
 // ------------------------------------------------------- early-exit units
@@ -542,10 +565,14 @@ __device__ __forceinline__ void argmax_unit_early(const StepParams& p, SharedSta
       int due = -1, a = -1;
       atomicMax(p.keys + r, k);
       fence_acq_rel();  // release
-      if (atomicAdd(p.rcount + r, 1u) == (unsigned)(p.C - 1)) {  // row r complete
+      const unsigned rc = atomicAdd(p.rcount + r, 1u);
+      if (rc >= (unsigned)p.C) atomicOr(p.err, PE_ERR_WORKSPACE);  // did not start at zero
+      if (rc == (unsigned)(p.C - 1)) {  // row r complete
         const unsigned long long kk = atomicExch(p.keys + r, 0ull);
         atomicExch(p.rcount + r, 0u);
-        const int am = (int)key_col(kk);
+        const uint32_t col = key_col(kk);
+        if (kk == 0ull || col >= (uint32_t)p.V) atomicOr(p.err, PE_ERR_WORKSPACE);
+        const int am = (int)col;
         p.amax_ws[r] = am;
         const int io = seg_begin(p, b);
         const int vb = seg_begin(p, b + 1) - io - 1 - p.Kp;
@@ -553,6 +580,12 @@ __device__ __forceinline__ void argmax_unit_early(const StepParams& p, SharedSta
         const unsigned long long bits = (1ull << j) | (match ? (1ull << (32 + j)) : 0ull);
         fence_acq_rel();  // release: the row's argmax before its done bit
         const unsigned long long old = atomicOr(p.state + b, bits);
+        // before this OR: done bits of other rows < K'+1 only, match bits of
+        // rows < K' only, and not this row's done bit
+        const unsigned long long legal =
+            (p.Kp == 31 ? 0xffffffffull : (1ull << (p.Kp + 1)) - 1ull) |
+            (((1ull << p.Kp) - 1ull) << 32);
+        if ((old & ~legal) || ((old >> j) & 1ull)) atomicOr(p.err, PE_ERR_WORKSPACE);
         const int a_new = settled(old | bits, p.Kp);
         if (settled(old, p.Kp) < 0 && a_new >= 0) {
           fence_acq_rel();  // acquire: the argmax of every row it settles on
@@ -567,7 +600,7 @@ __device__ __forceinline__ void argmax_unit_early(const StepParams& p, SharedSta
   __syncthreads();
   const int due = sh.last;
   const int a = sh.first;
-  if (due >= 0) request_epilogue<SyncAll, true>(p, sh, due, a);
+  if (due >= 0) request_epilogue<true>(p, sh, due, a);
 }
 
 // ------------------------------------------------------------------ X tiles
@@ -612,8 +645,11 @@ __device__ __forceinline__ void other_row(const StepParams& p, int i, int& t, in
   t = io + b * (p.K - 1) + (l < n - nr ? l : l + nr);
 }
 
-template <class S, int kSeg, int kCols>
-__device__ __forceinline__ void copy_unit(const StepParams& p, SharedState& sh, int u) {
+// Setup of a copy tile: thread i < nrows works out row i's two half rows
+// (source, destination, mode), writes a prompt row's metadata, and notes a
+// verified row's request for the hand-off.  Returns the tile's row count.
+__device__ __forceinline__ int copy_setup(const StepParams& p, SharedState& sh, int u,
+                                          bool& vtile_out) {
   const int tid = threadIdx.x;
   const bool vtile = u < p.n_vtile;  // a tile of verified rows
   const int i0 = (vtile ? u : u - p.n_vtile) * p.rows_per_unit;
@@ -683,7 +719,16 @@ __device__ __forceinline__ void copy_unit(const StepParams& p, SharedState& sh, 
     sh.dst[2 * tid + 1] = xr ? xr + p.nvh : nullptr;
   }
   if (tid == 0) sh.nbonus = 0;
-  S::sync();
+  vtile_out = vtile;
+  return nrows;
+}
+
+// Copy body, register path: kSeg half rows x kCols vectors per thread in
+// flight (eight 16-byte loads per thread).
+template <int kSeg, int kCols>
+__device__ __forceinline__ void copy_body_regs(const StepParams& p, const SharedState& sh,
+                                               int nrows) {
+  const int tid = threadIdx.x;
   const int nseg = 2 * nrows;  // kSeg half rows x kCols vectors per thread per batch
   for (int v0 = 0; v0 < p.nvh; v0 += kCols * kThreads) {
     for (int sg = 0; sg < nseg; sg += kSeg) {
@@ -713,19 +758,64 @@ __device__ __forceinline__ void copy_unit(const StepParams& p, SharedState& sh, 
       }
     }
   }
-  if (!vtile) return;
-  // Hand-off: count this tile's verified rows into their requests' words,
-  // ordered after every thread's stores of the tile (the barrier gathers
-  // them, the counting thread's release fence publishes them).  The tile
-  // that completes a request's count after its verdict was taken writes the
-  // bonus row (its embedding half with the bonus token); if the verdict
-  // comes later, the verdict writes it.
-  S::sync();
+}
+
+// Copy body, bulk path: one thread moves every half row of the tile through
+// the CTA's staging buffer (2 * rows_per_unit half rows of nvh vectors):
+// a bulk load per half row, completion on the CTA's barrier, then a bulk
+// store per half row.  Half rows to be zeroed (a token outside the table)
+// are written by all threads with plain stores.  `phase` is the parity of
+// the barrier's next phase (thread 0's copy).  verified: the tile's rows
+// take part in the bonus-row hand-off, so the stores must be complete and
+// ordered before the thread's later accesses when this returns.
+__device__ __forceinline__ void copy_body_bulk(const StepParams& p, SharedState& sh, int nrows,
+                                               uint4* stage, uint32_t& phase, bool verified) {
+  const int tid = threadIdx.x;
+  const int nseg = 2 * nrows;
+  const uint32_t seg_bytes = (uint32_t)p.nvh * 16u;
+  if (tid == 0) {
+    bulk_wait_read_all();  // the previous tile's stores have left the buffer
+    uint32_t bytes = 0;
+    for (int sg = 0; sg < nseg; ++sg)
+      if (sh.mode[sg] == kCopy) bytes += seg_bytes;
+    mbar_arrive_expect_tx(&sh.bar, bytes);
+    for (int sg = 0; sg < nseg; ++sg)
+      if (sh.mode[sg] == kCopy)
+        bulk_load(stage + (long long)sg * p.nvh, sh.src[sg], seg_bytes, &sh.bar);
+  }
+  for (int sg = 0; sg < nseg; ++sg)
+    if (sh.mode[sg] == kZero)
+      for (int v = tid; v < p.nvh; v += kThreads) sh.dst[sg][v] = make_uint4(0u, 0u, 0u, 0u);
+  if (tid == 0) {
+    if (mbar_wait(&sh.bar, phase)) {
+      for (int sg = 0; sg < nseg; ++sg)
+        if (sh.mode[sg] == kCopy) bulk_store(sh.dst[sg], stage + (long long)sg * p.nvh, seg_bytes);
+      bulk_commit();
+    } else {
+      atomicOr(p.err, PE_ERR_TIMEOUT);  // never expected: the loads did not land
+    }
+    phase ^= 1u;
+    if (verified) bulk_wait_all_visible();
+  }
+}
+
+// Hand-off of a verified-row tile: count this tile's verified rows into
+// their requests' words, ordered after every thread's stores of the tile
+// (the barrier gathers them, the counting thread's release fence publishes
+// them).  The tile that completes a request's count after its verdict was
+// taken writes the bonus row (its embedding half with the bonus token); if
+// the verdict comes later, the verdict writes it.
+__device__ __forceinline__ void copy_handoff(const StepParams& p, SharedState& sh, int nrows) {
+  const int tid = threadIdx.x;
+  __syncthreads();
   if (tid < nrows && sh.vreq[tid] >= 0) {
     const int b = sh.vreq[tid];
     fence_acq_rel();  // release
     const unsigned long long old = atomicAdd(p.xfer + b, 1ull);
-    if ((old & kXferCount) + 1 == (unsigned long long)(p.Kp + 1) && (old & kXferVerdict)) {
+    if (!xfer_legal(old, p.Kp, true)) {
+      atomicOr(p.err, PE_ERR_WORKSPACE);
+    } else if ((old & kXferCount) + 1 == (unsigned long long)(p.Kp + 1) &&
+               (old & kXferVerdict)) {
       atomicExch(p.xfer + b, 0ull);  // both sides are done: clear for the next call
       fence_acq_rel();  // acquire: other tiles' writes of the row come first
       const int e = atomicAdd(&sh.nbonus, 1);
@@ -733,7 +823,7 @@ __device__ __forceinline__ void copy_unit(const StepParams& p, SharedState& sh, 
       sh.btok[e] = (int)(uint32_t)(old >> 32);
     }
   }
-  S::sync();
+  __syncthreads();
   const int nb = sh.nbonus;
   for (int e = 0; e < nb; ++e) {
     const int tok = sh.btok[e];
@@ -744,24 +834,41 @@ __device__ __forceinline__ void copy_unit(const StepParams& p, SharedState& sh, 
   }
 }
 
-// Copy tile with eight loads per thread in flight: eight half rows at a time
-// when a half row is at most one vector per thread, else four half rows of
-// two vectors.
-template <class S>
-__device__ __forceinline__ void copy_tile(const StepParams& p, SharedState& sh, int u) {
-  if (p.nvh <= kThreads)
-    copy_unit<S, 8, 1>(p, sh, u);
+// Copy tile u.  Register path: eight loads per thread in flight, eight half
+// rows at a time when a half row is at most one vector per thread, else four
+// half rows of two vectors.  Bulk path: see copy_body_bulk.
+template <bool BULK>
+__device__ __forceinline__ void copy_tile(const StepParams& p, SharedState& sh, int u,
+                                          uint4* stage, uint32_t& phase) {
+  bool vtile;
+  const int nrows = copy_setup(p, sh, u, vtile);
+  __syncthreads();
+  if (BULK)
+    copy_body_bulk(p, sh, nrows, stage, phase, vtile);
+  else if (p.nvh <= kThreads)
+    copy_body_regs<8, 1>(p, sh, nrows);
   else
-    copy_unit<S, 4, 2>(p, sh, u);
+    copy_body_regs<4, 2>(p, sh, nrows);
+  if (vtile) copy_handoff(p, sh, nrows);
 }
 
 // ------------------------------------------------------------------- kernel
-template <int DT>
+// BULK: copy tiles through the dynamic shared-memory staging buffer.
+template <int DT, bool BULK>
 __global__ void __launch_bounds__(kThreads, 4) step_kernel(const StepParams p) {
+  extern __shared__ __align__(128) uint4 stage[];
   __shared__ SharedState sh;
   if (p.in_offsets && !offsets_valid(p.in_offsets, p.B, p.R, p.Kp + 1)) {
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.err, PE_ERR_OFFSETS);
     return;  // every CTA sees the same offsets and leaves without writing
+  }
+  uint32_t phase = 0;  // bulk tiles: parity of the barrier's next phase (thread 0)
+  if (BULK) {
+    if (threadIdx.x == 0) {
+      mbar_init(&sh.bar, 1);
+      mbar_init_fence();
+    }
+    __syncthreads();
   }
   // The first unit of each CTA is its own index; later units come from the
   // counter, which therefore hands out gridDim.x + 0, 1, 2, ...  A CTA takes
@@ -773,20 +880,27 @@ __global__ void __launch_bounds__(kThreads, 4) step_kernel(const StepParams p) {
     if (u < p.n_arg_units)
       argmax_unit<DT>(p, sh, u);
     else
-      copy_tile<SyncAll>(p, sh, u - p.n_arg_units);
+      copy_tile<BULK>(p, sh, u - p.n_arg_units, stage, phase);
     __syncthreads();
     if (threadIdx.x == 0) {
       // The counter hands out n_units - gridDim.x units, then one index past
       // the end to each CTA, after which that CTA never touches it again: the
       // CTA that receives the last index (n_units - 1) is the last to finish
-      // and resets the counter for the next call.
+      // and resets the counter for the next call.  A larger value means the
+      // counter did not start at zero: the CTA leaves.
       const unsigned v = atomicAdd(p.sched, 1u);
       if (v == (unsigned)p.n_units - 1u) atomicExch(p.sched, 0u);
-      sh.unit = (int)(gridDim.x + v);
+      unsigned next = gridDim.x + v;
+      if (v > (unsigned)p.n_units - 1u) {
+        atomicOr(p.err, PE_ERR_WORKSPACE);
+        next = (unsigned)p.n_units;
+      }
+      sh.unit = (int)next;
     }
     __syncthreads();
     q = sh.unit;
   }
+  if (BULK && threadIdx.x == 0) bulk_wait_all_visible();  // stores done before the CTA ends
 }
 
 // --------------------------------------------------- early-exit scheduling
@@ -797,12 +911,21 @@ __global__ void __launch_bounds__(kThreads, 4) step_kernel(const StepParams p) {
 // it is already known to mismatch at an earlier row, takes the next index
 // instead, alone, without holding the CTA at a barrier per skipped unit.
 
-// Unit at or after queue position q that is worth reading, or a value
-// >= n_units when the queue is exhausted (thread 0 only).
-__device__ __forceinline__ int skip_moot(const StepParams& p, int q) {
+// Next queue position (thread 0).  Every position below n_units is claimed
+// once, then each CTA makes one claim past the end and leaves, so a value
+// above n_units + gridDim.x - 1 means the counter did not start at zero.
+__device__ __forceinline__ unsigned claim_early(const StepParams& p) {
+  const unsigned v = atomicAdd(p.sched, 1u);
+  if (v > (unsigned)p.n_units + gridDim.x - 1u) atomicOr(p.err, PE_ERR_WORKSPACE);
+  return v;
+}
+
+// Unit at or after queue position q that is worth reading, or n_units when
+// the queue is exhausted (thread 0 only).
+__device__ __forceinline__ int skip_moot(const StepParams& p, unsigned q) {
   const int per_row = p.B * p.C;
-  while (q < p.n_units) {
-    const int u = unit_at(p, q);
+  while (q < (unsigned)p.n_units) {
+    const int u = unit_at(p, (int)q);
     if (u >= p.n_arg_units) return u;  // copy tile
     const int j = u / per_row;
     if (j == 0) return u;
@@ -810,7 +933,7 @@ __device__ __forceinline__ int skip_moot(const StepParams& p, int q) {
     const unsigned long long st = __ldcg(p.state + b);
     const unsigned done = (unsigned)st, match = (unsigned)(st >> 32);
     if (!(done & ~match & ((1u << j) - 1u))) return u;  // no earlier mismatch known
-    q = (int)atomicAdd(p.sched, 1u);                    // moot: take the next one
+    q = claim_early(p);                                 // moot: take the next one
   }
   return p.n_units;
 }
@@ -822,20 +945,22 @@ __global__ void __launch_bounds__(kThreads, 4) step_kernel_early(const StepParam
     if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.err, PE_ERR_OFFSETS);
     return;  // every CTA sees the same offsets and leaves without writing
   }
+  uint32_t phase = 0;  // (register copy tiles: unused)
   for (;;) {
-    if (threadIdx.x == 0) sh.unit = skip_moot(p, (int)atomicAdd(p.sched, 1u));
+    if (threadIdx.x == 0) sh.unit = skip_moot(p, claim_early(p));
     __syncthreads();
     const int u = sh.unit;
     if (u >= p.n_units) break;
     if (u < p.n_arg_units)
       argmax_unit_early<DT>(p, sh, u);
     else
-      copy_tile<SyncAll>(p, sh, u - p.n_arg_units);
+      copy_tile<false>(p, sh, u - p.n_arg_units, nullptr, phase);
     __syncthreads();
   }
   if (threadIdx.x == 0) {
     fence_acq_rel();  // release
     const unsigned done = atomicAdd(p.sched + 1, 1u);
+    if (done > gridDim.x - 1u) atomicOr(p.err, PE_ERR_WORKSPACE);  // did not start at zero
     sh.last = done == gridDim.x - 1;  // every other CTA has left
     if (sh.last) fence_acq_rel();  // acquire: their last accesses come first
   }
@@ -846,198 +971,13 @@ __global__ void __launch_bounds__(kThreads, 4) step_kernel_early(const StepParam
       p.rcount[i] = 0u;
       p.amax_ws[i] = 0;
     }
-    for (int i = threadIdx.x; i < p.B; i += kThreads) p.state[i] = 0ull;
+    // every request has settled by now (its rows are read in order up to its
+    // first mismatch); one that has not lost units to a dirty counter
+    for (int i = threadIdx.x; i < p.B; i += kThreads) {
+      if (settled(p.state[i], p.Kp) < 0) atomicOr(p.err, PE_ERR_WORKSPACE);
+      p.state[i] = 0ull;
+    }
     if (threadIdx.x == 0) {
-      atomicExch(p.sched, 0u);
-      atomicExch(p.sched + 1, 0u);
-    }
-  }
-}
-
-// ------------------------------------------------ pipelined (bulk-copy) kernel
-// One producer warp streams every argmax chunk into a ring of shared-memory
-// stages with cp.async.bulk (one instruction per 16 KiB, completion counted on
-// an mbarrier), running ahead across unit boundaries; eight consumer warps
-// reduce each stage from shared memory, hand it back through a second
-// mbarrier, and do the unit ends, epilogues and X tiles exactly as the
-// register-streaming kernel does.  Bytes in flight are bounded by the ring
-// (STAGES x 16 KiB per CTA), not by registers, and never stop while the
-// consumers finish a unit.
-constexpr int kTmaThreads = kThreads + 32;  // 8 consumer warps + 1 producer warp
-constexpr int kStageBytes = 16384;
-constexpr int kStageVecs = kStageBytes / 16;
-
-enum StageKind { kStageArgmax = 0, kStageCopy = 1, kStageStop = 2 };
-struct StageInfo {
-  int kind, unit, v, n, last;
-};
-
-// Producer (one thread): hand out units in order and fill the ring.
-template <int STAGES>
-__device__ __forceinline__ void produce(const StepParams& p, uint4* ring, uint64_t* full,
-                                        uint64_t* empty, StageInfo* info) {
-  const uint64_t pol = l2_evict_first_policy();
-  int stage = 0;
-  uint32_t phase = 0;
-  bool ok = true;
-  int pend[STAGES];  // parity of the last phase a copy was issued for, or -1
-#pragma unroll
-  for (int s = 0; s < STAGES; ++s) pend[s] = -1;
-  int q = blockIdx.x;  // queue position; unit_at gives the unit
-  for (;;) {
-    const bool stop = q >= p.n_units;
-    const int u = stop ? p.n_units : unit_at(p, q);
-    const int next = stop ? 0 : (int)(gridDim.x + atomicAdd(p.sched, 1u));
-    if (stop || u >= p.n_arg_units) {
-      if (!(ok = mbar_wait(&empty[stage], phase ^ 1))) break;
-      info[stage] = StageInfo{stop ? kStageStop : kStageCopy, stop ? 0 : u - p.n_arg_units,
-                              0, 0, 0};
-      mbar_arrive(&full[stage]);
-      if (++stage == STAGES) {
-        stage = 0;
-        phase ^= 1;
-      }
-      if (stop) break;
-    } else {
-      const int r = u / p.C;
-      const int c = u - r * p.C;
-      const char* rowp = logits_row(p, r);
-      const uint4* row = reinterpret_cast<const uint4*>(rowp);
-      const int v_lo = c * p.chunk_vecs;
-      const int v_hi = rowp ? min(v_lo + p.chunk_vecs, p.nvec) : v_lo;  // bad index: nothing
-      if (!rowp && c == 0) atomicOr(p.err, PE_ERR_ROW_RANGE);
-      int v = v_lo;
-      do {  // a chunk with no whole vector still sends one empty piece
-        const int n = max(0, min(kStageVecs, v_hi - v));
-        if (!(ok = mbar_wait(&empty[stage], phase ^ 1))) break;
-        info[stage] = StageInfo{kStageArgmax, u, v, n, v + n >= v_hi ? 1 : 0};
-        if (n > 0) {
-          mbar_arrive_expect_tx(&full[stage], (uint32_t)n * 16u);
-          bulk_load(ring + (long long)stage * kStageVecs, row + v, (uint32_t)n * 16u,
-                    &full[stage], pol);
-          pend[stage] = (int)phase;
-        } else {
-          mbar_arrive(&full[stage]);
-        }
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1;
-        }
-        v += kStageVecs;
-      } while (v < v_hi);
-      if (!ok) break;
-    }
-    q = next;
-  }
-  if (!ok) {
-    atomicOr(p.err, PE_ERR_TIMEOUT);
-    // let every copy already issued land before the CTA leaves (bounded)
-    for (int s = 0; s < STAGES; ++s)
-      if (pend[s] >= 0) mbar_wait(&full[s], (uint32_t)pend[s]);
-  }
-}
-
-// Consumers (eight warps): reduce stages in ring order.
-template <int DT, int STAGES>
-__device__ __forceinline__ void consume(const StepParams& p, SharedState& sh, const uint4* ring,
-                                        uint64_t* full, uint64_t* empty,
-                                        const StageInfo* info) {
-  using E = Elem<DT>;
-  const int tid = threadIdx.x;
-  const int lane = tid & 31;
-  int stage = 0;
-  uint32_t phase = 0;
-  float m = 0.f;
-  uint4 q = make_uint4(0u, 0u, 0u, 0u);
-  int qv = -1;
-  for (int iter = 0;; ++iter) {
-    // one thread waits (bounded) and tells the others, so that all consumers
-    // take the same branch and meet at the same named barriers; two slots,
-    // so thread 0 never overwrites a verdict another thread has yet to read
-    if (tid == 0) sh.verdict[iter & 1] = mbar_wait(&full[stage], phase) ? 1 : 0;
-    SyncConsumers::sync();
-    if (!sh.verdict[iter & 1]) {
-      if (tid == 0) atomicOr(p.err, PE_ERR_TIMEOUT);
-      break;
-    }
-    mbar_wait(&full[stage], phase);  // completed: returns at once, orders this thread
-    const StageInfo in = info[stage];
-    if (in.kind == kStageStop) break;
-    if (in.kind == kStageCopy) {
-      copy_unit<SyncConsumers, 8, 2>(p, sh, in.unit);
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);
-    } else {
-      const uint4* buf = ring + (long long)stage * kStageVecs;
-      uint4 x[kStageVecs / kThreads];
-#pragma unroll
-      for (int k = 0; k < kStageVecs / kThreads; ++k) {
-        const int i = k * kThreads + tid;
-        x[k] = i < in.n ? buf[i] : E::neg_inf();
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&empty[stage]);  // this warp is done with the stage
-#pragma unroll
-      for (int k = 0; k < kStageVecs / kThreads; ++k) {
-#ifdef PE_CHECKED
-        if (k * kThreads + tid < in.n && E::has_nan(x[k])) atomicOr(p.err, PE_ERR_NAN);
-#endif
-        const float vm = E::vmax(x[k]);
-        const bool valid = k * kThreads + tid < in.n;
-        if (valid && (qv < 0 || vm > m)) {  // pieces and k run in increasing column order
-          m = vm;
-          q = x[k];
-          qv = in.v + k * kThreads + tid;
-        }
-      }
-      if (in.last) {
-        const int r = in.unit / p.C;
-        const int c = in.unit - r * p.C;
-        const unsigned long long key =
-            qv >= 0 ? make_key(m, (uint32_t)(qv * E::kPerVec + E::first_equal(q, m))) : 0ull;
-        finish_argmax_unit<SyncConsumers, DT>(p, sh, r, c, logits_row(p, r), key);
-        qv = -1;
-      }
-    }
-    if (++stage == STAGES) {
-      stage = 0;
-      phase ^= 1;
-    }
-  }
-}
-
-template <int DT, int STAGES, int MINB>
-__global__ void __launch_bounds__(kTmaThreads, MINB) step_kernel_tma(const StepParams p) {
-  extern __shared__ __align__(128) unsigned char ring_raw[];
-  __shared__ SharedState sh;
-  __shared__ __align__(8) uint64_t full[STAGES];
-  __shared__ __align__(8) uint64_t empty[STAGES];
-  __shared__ StageInfo info[STAGES];
-  if (p.in_offsets && !offsets_valid(p.in_offsets, p.B, p.R, p.Kp + 1)) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.err, PE_ERR_OFFSETS);
-    return;
-  }
-  const int tid = threadIdx.x;
-  if (tid == 0) {
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], kWarps);
-    }
-    mbar_init_fence();
-  }
-  __syncthreads();
-  if ((tid >> 5) == kWarps) {
-    if ((tid & 31) == 0)
-      produce<STAGES>(p, reinterpret_cast<uint4*>(ring_raw), full, empty, info);
-    __syncwarp();
-  } else {
-    consume<DT, STAGES>(p, sh, reinterpret_cast<const uint4*>(ring_raw), full, empty, info);
-  }
-  __syncthreads();
-  if (tid == 0) {
-    fence_acq_rel();  // release
-    const unsigned done = atomicAdd(p.sched + 1, 1u);
-    if (done == gridDim.x - 1) {
       atomicExch(p.sched, 0u);
       atomicExch(p.sched + 1, 0u);
     }
@@ -1084,42 +1024,39 @@ void plan_argmax(pe::StepParams& p, int elt, int rows, int grid_max, int batches
     p.chunk_vecs = chunk;
     p.C = (p.nvec + chunk - 1) / chunk;
   }
-  p.n_arg_units = rows * p.C;
+  // -1 when the units (plus one final claim per CTA) would not fit an int
+  const long long units = (long long)rows * p.C;
+  p.n_arg_units = units + grid_max > 0x7fffffffLL ? -1 : (int)units;
 }
 
-template <int DT, int STAGES, int MINB>
-int launch_tma(const pe::StepParams& p, int grid, cudaStream_t stream) {
-  static std::atomic<unsigned long long> attr_done{0};
-  const int smem = STAGES * pe::kStageBytes;
-  if (!pe_host::allow_smem(pe::step_kernel_tma<DT, STAGES, MINB>, smem, attr_done)) return PE_ECUDA;
-  pe::step_kernel_tma<DT, STAGES, MINB><<<grid, pe::kTmaThreads, smem, stream>>>(p);
-  return pe_host::launch_status();
+// Staging budget of a bulk-copy tile per CTA (four CTAs per SM share the
+// SM's shared memory with their static state).
+constexpr int kBulkStageBytes = 48 * 1024;
+
+// X rows a bulk-copy tile can stage for half rows of `half_bytes` bytes (0:
+// not even one, the register path is used).
+int bulk_rows_for(long long half_bytes, int rows_per_unit) {
+  const long long fit = kBulkStageBytes / (2 * half_bytes);
+  return (int)(fit < rows_per_unit ? fit : rows_per_unit);
 }
 
-// Grid of the chosen kernel variant: register streaming (ctas_per_sm CTAs
-// of 256 threads per SM) or the bulk-copy pipeline (1 CTA with a 12-stage
-// ring, or 2 CTAs with 6 stages each, per SM).
-int grid_max_for(const pe_host::Tuning& tn, const pe_host::DeviceInfo& dev) {
-  if (tn.variant == 2) return dev.sm_count * (tn.ctas_per_sm >= 2 ? 2 : 1);
-  return dev.sm_count * tn.ctas_per_sm;
-}
-
-
-int launch(const pe::StepParams& p, int dtype, int grid, const pe_host::Tuning& tn,
-           cudaStream_t stream) {
-  if (tn.variant == 2) {
-    const bool two = tn.ctas_per_sm >= 2;
-    if (dtype == PE_BF16)
-      return two ? launch_tma<PE_BF16, 6, 2>(p, grid, stream)
-                 : launch_tma<PE_BF16, 12, 1>(p, grid, stream);
-    return two ? launch_tma<PE_F32, 6, 2>(p, grid, stream)
-               : launch_tma<PE_F32, 12, 1>(p, grid, stream);
+template <int DT>
+int launch_full(const pe::StepParams& p, int grid, cudaStream_t stream) {
+  if (p.bulk_rows > 0) {
+    static std::atomic<unsigned long long> attr_done{0};
+    const int smem = p.bulk_rows * 2 * p.nvh * 16;
+    if (!pe_host::allow_smem(pe::step_kernel<DT, true>, kBulkStageBytes, attr_done))
+      return PE_ECUDA;
+    pe::step_kernel<DT, true><<<grid, pe::kThreads, smem, stream>>>(p);
+  } else {
+    pe::step_kernel<DT, false><<<grid, pe::kThreads, 0, stream>>>(p);
   }
-  if (dtype == PE_BF16)
-    pe::step_kernel<PE_BF16><<<grid, pe::kThreads, 0, stream>>>(p);
-  else
-    pe::step_kernel<PE_F32><<<grid, pe::kThreads, 0, stream>>>(p);
   return pe_host::launch_status();
+}
+
+int launch(const pe::StepParams& p, int dtype, int grid, cudaStream_t stream) {
+  return dtype == PE_BF16 ? launch_full<PE_BF16>(p, grid, stream)
+                          : launch_full<PE_F32>(p, grid, stream);
 }
 
 int launch_early(const pe::StepParams& p, int dtype, int grid, cudaStream_t stream) {
@@ -1179,12 +1116,13 @@ int pe_verify_greedy(const void* logits, int dtype, int64_t row_stride, int32_t 
   p.target_argmax = target_argmax;
   p.err = err;
   const int rows = B * (Kp + 1);
-  const int grid_max = grid_max_for(tn, dev);
+  const int grid_max = dev.sm_count * tn.ctas_per_sm;
   plan_argmax(p, elt, rows, grid_max, tn.chunk_batches);
   p.n_units = p.n_arg_units;
+  if (p.n_units < 0) return PE_EINVAL;  // more units than an int counts
   bind_workspace(p, workspace, rows, B);
   const int grid = p.n_units < grid_max ? p.n_units : grid_max;
-  return launch(p, dtype, grid, tn, static_cast<cudaStream_t>(stream));
+  return launch(p, dtype, grid, static_cast<cudaStream_t>(stream));
 }
 
 int pe_draft_readout(const void* logits, int dtype, int64_t row_stride, int32_t rows,
@@ -1215,12 +1153,13 @@ int pe_draft_readout(const void* logits, int dtype, int64_t row_stride, int32_t 
   p.rows_total = rows;
   p.bonus_token = out_tokens;
   p.err = err;
-  const int grid_max = grid_max_for(tn, dev);
+  const int grid_max = dev.sm_count * tn.ctas_per_sm;
   plan_argmax(p, elt, n, grid_max, tn.chunk_batches);
   p.n_units = p.n_arg_units;
+  if (p.n_units < 0) return PE_EINVAL;  // more units than an int counts
   bind_workspace(p, workspace, n, n);
   const int grid = p.n_units < grid_max ? p.n_units : grid_max;
-  return launch(p, dtype, grid, tn, static_cast<cudaStream_t>(stream));
+  return launch(p, dtype, grid, static_cast<cudaStream_t>(stream));
 }
 
 namespace {
@@ -1319,20 +1258,25 @@ int step_common(const pe_step_args* a, void* stream, bool early) {
     early = false;
     p.mask_unread = 1;
   }
-  // the early-exit step runs on the register-streaming kernel
-  pe_host::Tuning tk = tn;
-  if (early) tk.variant = 1;
-  const int grid_max = grid_max_for(tk, dev);
-  plan_argmax(p, elt, rows, grid_max, tk.chunk_batches);
-  p.rows_per_unit = tk.rows_per_unit;
+  const int grid_max = dev.sm_count * tn.ctas_per_sm;
+  plan_argmax(p, elt, rows, grid_max, tn.chunk_batches);
+  // bulk-copy tiles (variant 2; the early-exit kernel copies through
+  // registers): as many rows per tile as the staging buffer holds
+  p.rows_per_unit = tn.rows_per_unit;
+  if (tn.variant == 2 && !early) {
+    p.bulk_rows = bulk_rows_for((long long)p.nvh * 16, tn.rows_per_unit);
+    if (p.bulk_rows > 0) p.rows_per_unit = p.bulk_rows;
+  }
   p.rv = rows;  // verified rows: tiles of their own
   p.n_vtile = (p.rv + p.rows_per_unit - 1) / p.rows_per_unit;
-  p.vfirst = tk.queue_order != 2;
+  p.vfirst = tn.queue_order != 2;
   p.n_copy_units = p.n_vtile + (p.T - p.rv + p.rows_per_unit - 1) / p.rows_per_unit;
-  p.n_units = p.n_arg_units + p.n_copy_units;
+  const long long n_units = (long long)p.n_arg_units + p.n_copy_units;
+  if (p.n_arg_units < 0 || n_units + grid_max > 0x7fffffffLL) return PE_EINVAL;
+  p.n_units = (int)n_units;
   bind_workspace(p, a->workspace, rows, B);
   const int grid = p.n_units < grid_max ? p.n_units : grid_max;
   if (early) return launch_early(p, a->logits_dtype, grid, static_cast<cudaStream_t>(stream));
-  return launch(p, a->logits_dtype, grid, tk, static_cast<cudaStream_t>(stream));
+  return launch(p, a->logits_dtype, grid, static_cast<cudaStream_t>(stream));
 }
 }  // namespace

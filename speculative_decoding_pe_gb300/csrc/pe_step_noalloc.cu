@@ -34,7 +34,10 @@ std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices];  // device address of the array, per device
 
 // Device address of the scratch on the current device.  The first call on a
-// device looks it up (which may load this library's GPU code on that device).
+// device looks it up (which may load this library's GPU code on that device)
+// and keeps it until the process exits: it stays valid as long as the
+// device's primary context lives, i.e. unless the program resets the device
+// (cudaDeviceReset), after which this entry point must not be used there.
 int scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PE_ECUDA;

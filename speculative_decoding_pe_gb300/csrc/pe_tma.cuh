@@ -1,24 +1,17 @@
 // Shared-memory barriers and bulk asynchronous copies (sm_90+ PTX, used on
-// sm_103a): the pieces of a producer / consumer pipeline that streams global
-// memory into a shared-memory ring.
+// sm_103a): what the bulk-copy X tiles of the fused step need to move half
+// rows global -> shared -> global without passing through registers.
 //
-// Every wait is bounded: it gives up after kSpinLimit polls and reports
-// failure to the caller, which raises PE_ERR_TIMEOUT and leaves.  In a
-// correct pipeline no wait ever runs out.
+// The one wait (on a CTA's own barrier, for its own bulk loads) is bounded:
+// it gives up after kWaitLimitNs and reports failure to the caller, which
+// raises PE_ERR_TIMEOUT.  In a correct program it never runs out.
 #pragma once
 
 #include <stdint.h>
 
 namespace pe {
 
-constexpr int kSpinLimit = 1 << 26;
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
-
-__device__ __forceinline__ unsigned long long global_ns() {
-  unsigned long long t;
-  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-  return t;
-}
+constexpr unsigned long long kWaitLimitNs = 50000000ull;  // 50 ms
 
 __device__ __forceinline__ uint32_t smem_addr(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -32,10 +25,6 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
 // Make barrier initialisation visible to the asynchronous (bulk copy) proxy.
 __device__ __forceinline__ void mbar_init_fence() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 // Arrive and announce `bytes` more bytes that bulk copies will deliver.
@@ -58,41 +47,48 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Wait until the phase with parity `parity` of `bar` has completed; false
-// when the bound (kSpinLimit polls or kWaitLimitNs) runs out.
+// when kWaitLimitNs of global time pass first.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
-  for (int i = 0; i < kSpinLimit; ++i) {
+  for (;;) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 255) == 255 && global_ns() - t0 > kWaitLimitNs) return false;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
   }
-  return false;
-}
-
-// L2 policy for data read exactly once (evicted first).
-__device__ __forceinline__ uint64_t l2_evict_first_policy() {
-  uint64_t pol;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
 }
 
 // Bulk copy of `bytes` (multiple of 16, both addresses 16-byte aligned) from
 // global memory into this CTA's shared memory; completion is counted on
 // `bar` as transaction bytes.
 __device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
-                                          uint64_t* bar, uint64_t policy) {
+                                          uint64_t* bar) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
-      "[%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(smem_dst)),
-      "l"(gsrc), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1], %2, [%3];" ::"r"(smem_addr(smem_dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
 
-// Named barrier over the first `nthreads` threads of the CTA (id 1; id 0 is
-// __syncthreads).
-template <int kCount>
-__device__ __forceinline__ void named_sync() {
-  asm volatile("bar.sync 1, %0;" ::"n"(kCount) : "memory");
+// Bulk copy of `bytes` from this CTA's shared memory to global memory, in
+// the issuing thread's current bulk group.
+__device__ __forceinline__ void bulk_store(void* gdst, const void* smem_src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_addr(smem_src)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// Every bulk store this thread committed has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// Every bulk store this thread committed has completed its global writes;
+// the proxy fence then orders them before this thread's later generic
+// accesses (a release fence, a plain store to the same bytes).
+__device__ __forceinline__ void bulk_wait_all_visible() {
+  asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 }  // namespace pe

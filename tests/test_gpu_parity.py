@@ -45,9 +45,12 @@ class tuned:
         _native.set_tuning(**self.before)
 
 
-VARIANTS = [dict(variant=1), dict(variant=2), dict(variant=1, queue_order=2),
-            dict(variant=2, queue_order=2)]
-VARIANT_IDS = ["regs", "pipeline", "regs_tiles_last", "pipeline_tiles_last"]
+# copy tiles through registers / bulk copies; verified-row tiles first
+# (queue_order 1: the verdict usually writes the bonus row) or every tile
+# after the argmax chunks (2, the default: the tiles usually write it)
+VARIANTS = [dict(variant=1, queue_order=1), dict(variant=2, queue_order=1),
+            dict(variant=1, queue_order=2), dict(variant=2, queue_order=2)]
+VARIANT_IDS = ["regs_vfirst", "bulk_vfirst", "regs", "bulk"]
 
 
 # ------------------------------------------------------------ full sizes
@@ -172,7 +175,7 @@ def _tie_rows(V, dtype):
 @pytest.mark.parametrize("tuning", [dict(), dict(ctas_per_sm=1, chunk_batches=1),
                                     dict(variant=2, ctas_per_sm=1),
                                     dict(variant=2, ctas_per_sm=2, chunk_batches=1)],
-                         ids=["default", "coarse", "pipeline", "pipeline_fine"])
+                         ids=["default", "coarse", "variant2", "variant2_fine"])
 def test_verify_argmax_ties(V, dtype, pad, tuning):
     rows = _tie_rows(V, dtype)
     ref = oracle.argmax_rows(rows)
