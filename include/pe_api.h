@@ -366,6 +366,15 @@ typedef struct pe_tuning {
                               requests the serial row waves cost more than
                               the extra bytes.  Default 128; -1 sets 0
                               (always the early-exit kernel) */
+  int32_t single_pass;     /* 1 (default): a step whose work units fit one
+                              per co-resident CTA (few requests) runs as a
+                              cooperative launch in which every CTA does one
+                              unit and leaves: chunk keys go to slots in the
+                              workspace, and the CTA of a request's last
+                              chunk collects them (a bounded wait on the
+                              other CTAs, all resident by construction)
+                              instead of merging and counting through
+                              atomics; same outputs.  -1: never */
 } pe_tuning;
 int pe_get_tuning(pe_tuning* out /* host */);
 int pe_set_tuning(const pe_tuning* in /* host */);

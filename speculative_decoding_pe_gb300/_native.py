@@ -72,7 +72,8 @@ class StepArgs(ctypes.Structure):
 class Tuning(ctypes.Structure):
     """Mirror of pe_tuning."""
     _fields_ = [("ctas_per_sm", i32), ("chunk_batches", i32), ("rows_per_unit", i32),
-                ("variant", i32), ("queue_order", i32), ("early_full_read_mb", i32)]
+                ("variant", i32), ("queue_order", i32), ("early_full_read_mb", i32),
+                ("single_pass", i32)]
 
 
 _lock = threading.Lock()

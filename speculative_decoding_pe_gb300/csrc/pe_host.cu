@@ -17,6 +17,7 @@ std::atomic<int> g_rows_per_unit{4};
 std::atomic<int> g_variant{1};
 std::atomic<int> g_queue_order{2};
 std::atomic<int> g_early_full_read_mb{128};
+std::atomic<int> g_single_pass{1};
 }  // namespace
 
 int device_info(DeviceInfo* out) {
@@ -42,6 +43,7 @@ Tuning tuning() {
   t.variant = g_variant.load(std::memory_order_relaxed);
   t.queue_order = g_queue_order.load(std::memory_order_relaxed);
   t.early_full_read_mb = g_early_full_read_mb.load(std::memory_order_relaxed);
+  t.single_pass = g_single_pass.load(std::memory_order_relaxed);
   return t;
 }
 
@@ -63,6 +65,7 @@ int pe_get_tuning(pe_tuning* out) {
   out->variant = t.variant;
   out->queue_order = t.queue_order;
   out->early_full_read_mb = t.early_full_read_mb;
+  out->single_pass = t.single_pass;
   return PE_OK;
 }
 
@@ -75,12 +78,14 @@ int pe_set_tuning(const pe_tuning* in) {
   if (in->variant < 0 || in->variant > 2) return PE_EINVAL;
   if (in->queue_order < 0 || in->queue_order > 2) return PE_EINVAL;
   if (in->early_full_read_mb < -1 || in->early_full_read_mb > 65536) return PE_EINVAL;
+  if (in->single_pass < -1 || in->single_pass > 1) return PE_EINVAL;
   if (in->ctas_per_sm) pe_host::g_ctas_per_sm.store(in->ctas_per_sm);
   if (in->chunk_batches) pe_host::g_chunk_batches.store(in->chunk_batches);
   if (in->rows_per_unit) pe_host::g_rows_per_unit.store(in->rows_per_unit);
   if (in->variant) pe_host::g_variant.store(in->variant);
   if (in->queue_order) pe_host::g_queue_order.store(in->queue_order);
   if (in->early_full_read_mb) pe_host::g_early_full_read_mb.store(in->early_full_read_mb < 0 ? 0 : in->early_full_read_mb);
+  if (in->single_pass) pe_host::g_single_pass.store(in->single_pass);
   return PE_OK;
 }
 

@@ -51,6 +51,18 @@ __device__ __forceinline__ unsigned long long global_ns() {
   return t;
 }
 
+// Strong (relaxed, device-scope) 64-bit store and load: single-copy atomic,
+// so a reader polling the word sees either its old value or the whole new
+// one.  Used where the word itself is the message (no other data to order).
+__device__ __forceinline__ void st_relaxed(unsigned long long* a, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(a), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long* a) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
+  return v;
+}
+
 // Total order on non-NaN floats as unsigned integers, with -0.0 == +0.0.
 __device__ __forceinline__ uint32_t ordered_bits(float f) {
   uint32_t b = __float_as_uint(f);
@@ -147,6 +159,7 @@ struct Tuning {
   int variant;
   int queue_order;
   int early_full_read_mb;
+  int single_pass;
 };
 Tuning tuning();
 
@@ -157,7 +170,9 @@ inline int launch_status() {
 }
 
 // Dynamic shared memory above 48 KiB must be opted into once per kernel and
-// device (a host-side attribute; no synchronisation).
+// device (a host-side attribute; no synchronisation).  The kernel also asks
+// for the largest shared-memory carveout, so that the occupancy it was
+// sized for (several such CTAs per SM) is not cut by a larger L1.
 template <class K>
 bool allow_smem(K kernel, int bytes, std::atomic<unsigned long long>& done_mask) {
   int dev = 0;
@@ -165,7 +180,9 @@ bool allow_smem(K kernel, int bytes, std::atomic<unsigned long long>& done_mask)
   const unsigned long long bit = 1ull << dev;
   if (done_mask.load(std::memory_order_relaxed) & bit) return true;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
-      cudaSuccess)
+          cudaSuccess ||
+      cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared) != cudaSuccess)
     return false;
   done_mask.fetch_or(bit);
   return true;

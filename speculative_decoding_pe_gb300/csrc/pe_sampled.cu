@@ -363,16 +363,6 @@ __device__ __forceinline__ float2 unpack_partial(unsigned long long w) {
   return make_float2(__uint_as_float((uint32_t)(w >> 32) ^ kPartialMark),
                      __uint_as_float((uint32_t)w));
 }
-// Strong (relaxed, device-scope) 64-bit store and load: single-copy atomic,
-// so a poller sees either zero or the whole word.
-__device__ __forceinline__ void st_relaxed(unsigned long long* a, unsigned long long v) {
-  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(a), "l"(v) : "memory");
-}
-__device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long* a) {
-  unsigned long long v;
-  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");
-  return v;
-}
 
 // Accepted length of request b from its rows' draft-token probabilities.
 // Leaves the workspace zeroed except the normalisers the residual draw of

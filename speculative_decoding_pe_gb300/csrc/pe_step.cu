@@ -53,6 +53,7 @@
 //    known mismatch (step_kernel_early); with a small logits footprint the
 //    host serves it with the full read instead, the epilogue writing -1 to
 //    target_argmax after a_b.
+#include "pe_argmax.cuh"
 #include "pe_internal.cuh"
 #include "pe_tma.cuh"
 #include "pe_workspace.cuh"
@@ -100,6 +101,7 @@ struct StepParams {
   unsigned long long* xfer;   // per-request bonus-row hand-off word
   uint32_t* rcount;           // early exit: finished chunks per row
   int32_t* amax_ws;           // early exit: argmax of each completed row
+  unsigned long long* slots;  // single pass: chunk key of each argmax unit
   uint32_t* err;
 };
 
@@ -107,6 +109,7 @@ enum SegMode { kSkip = 0, kCopy = 1, kZero = 2 };
 
 struct SharedState {
   unsigned long long red[kWarps];
+  unsigned long long rowkey[PE_MAX_KP + 1];  // single pass: the rows' keys
   uint64_t bar;                // bulk-copy tiles: completion of the tile's loads
   int unit;
   int last;
@@ -170,62 +173,6 @@ __device__ __forceinline__ int seg_begin(const StepParams& p, int b) {
   return p.in_offsets ? __ldg(p.in_offsets + b) : b * (p.Kp + 1);
 }
 
-// ------------------------------------------------------------ element types
-template <int DT>
-struct Elem;
-
-template <>
-struct Elem<PE_BF16> {
-  static constexpr int kPerVec = 8;
-  __device__ static __forceinline__ bool has_nan(uint4 q) { return bf16x8_has_nan(q); }
-  __device__ static __forceinline__ uint4 neg_inf() {
-    return make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u);
-  }
-  // max of the 8 elements of a vector (exact: max returns one of its inputs)
-  __device__ static __forceinline__ float vmax(uint4 q) {
-    const uint32_t w = bf16x2_max(bf16x2_max(q.x, q.y), bf16x2_max(q.z, q.w));
-    return fmaxf(bf16_lo(w), bf16_hi(w));
-  }
-  // lowest element of q equal to v (v is known to occur in q)
-  __device__ static __forceinline__ int first_equal(uint4 q, float v) {
-    int e = 7;
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int i = 3; i >= 0; --i) {
-      if (bf16_hi(w[i]) == v) e = 2 * i + 1;
-      if (bf16_lo(w[i]) == v) e = 2 * i;
-    }
-    return e;
-  }
-  __device__ static __forceinline__ float scalar(const char* row, int col) {
-    uint16_t h = __ldg(reinterpret_cast<const unsigned short*>(row) + col);
-    return __uint_as_float(((uint32_t)h) << 16);
-  }
-};
-
-template <>
-struct Elem<PE_F32> {
-  static constexpr int kPerVec = 4;
-  __device__ static __forceinline__ bool has_nan(uint4 q) { return f32x4_has_nan(q); }
-  __device__ static __forceinline__ uint4 neg_inf() {
-    return make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
-  }
-  __device__ static __forceinline__ float vmax(uint4 q) {
-    return fmaxf(fmaxf(__uint_as_float(q.x), __uint_as_float(q.y)),
-                 fmaxf(__uint_as_float(q.z), __uint_as_float(q.w)));
-  }
-  __device__ static __forceinline__ int first_equal(uint4 q, float v) {
-    int e = 3;
-    if (__uint_as_float(q.z) == v) e = 2;
-    if (__uint_as_float(q.y) == v) e = 1;
-    if (__uint_as_float(q.x) == v) e = 0;
-    return e;
-  }
-  __device__ static __forceinline__ float scalar(const char* row, int col) {
-    return __ldg(reinterpret_cast<const float*>(row) + col);
-  }
-};
-
 // ------------------------------------------------------------------ epilogue
 // Runs in the CTA that finished the last argmax chunk of request b.  Its
 // global traffic is two dependent round trips: (1) the row keys (exchanged
@@ -234,12 +181,20 @@ struct Elem<PE_F32> {
 // the block-table entries of the kept slots with the metadata stores; then,
 // only when the request's verified-row tiles are already done, the bonus
 // row's embedding half.
-// EARLY: the accepted length `a_known` is already settled (early-exit step);
-// rows 0..a_known are read from the completed-row results and later rows,
-// which may never have been read, report -1.
-template <bool EARLY = false>
+// Where the row results come from:
+//  kKeysInWorkspace: the rows' merged keys in the workspace (exchanged with
+//    0) and the request's unit count (reset);
+//  kRowsSettled: early exit -- the accepted length `a_known` is already
+//    settled; rows 0..a_known are read from the completed-row results and
+//    later rows, which may never have been read, report -1;
+//  kKeysInShared: single pass -- the collecting CTA left the rows' keys in
+//    sh.rowkey and the drafts and positions in sh.tok / sh.pos.
+enum KeySource { kKeysInWorkspace = 0, kRowsSettled = 1, kKeysInShared = 2 };
+
+template <int SRC = kKeysInWorkspace>
 __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedState& sh,
                                                  int b, int a_known = -1) {
+  constexpr bool EARLY = SRC == kRowsSettled;
   const int tid = threadIdx.x;
   const int Kp = p.Kp;
   const int nr = Kp + 1;  // verified rows (<= 256 = threads)
@@ -247,22 +202,26 @@ __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedStat
   const int n = seg_begin(p, b + 1) - io;
   const int vb = n - 1 - Kp;  // segment row of the first verified row
   if (tid < nr) {
-    if (EARLY) {
+    if (SRC == kRowsSettled) {
       sh.amax[tid] = tid <= a_known ? __ldcg(p.amax_ws + (long long)b * nr + tid) : -1;
-    } else {
+    } else if (SRC == kKeysInWorkspace) {
       const unsigned long long k = atomicExch(p.keys + (long long)b * nr + tid, 0ull);
       const uint32_t col = key_col(k);
       // a merged key names a column of the row (0: a readout row outside the
       // logits, which holds no element)
       if (k != 0ull && col >= (uint32_t)p.V) atomicOr(p.err, PE_ERR_WORKSPACE);
       sh.amax[tid] = (int)col;
+    } else {
+      sh.amax[tid] = (int)key_col(sh.rowkey[tid]);
     }
-    if (tid < Kp) sh.tok[tid] = __ldg(p.in_tokens + io + vb + tid + 1);  // draft d_{tid+1}
-    if (p.full) sh.pos[tid] = __ldg(p.in_positions + io + vb + tid);
+    if (SRC != kKeysInShared) {
+      if (tid < Kp) sh.tok[tid] = __ldg(p.in_tokens + io + vb + tid + 1);  // draft d_{tid+1}
+      if (p.full) sh.pos[tid] = __ldg(p.in_positions + io + vb + tid);
+    }
   }
   if (tid == 0) {
     sh.first = EARLY ? a_known : Kp;
-    if (!EARLY) atomicExch(p.count + b, 0u);
+    if (SRC == kKeysInWorkspace) atomicExch(p.count + b, 0u);
   }
   __syncthreads();
   // accepted length: first draft that differs from the target's choice
@@ -370,61 +329,6 @@ __device__ __forceinline__ void finish_argmax_unit(const StepParams& p, SharedSt
                                                    int c, const char* rowp,
                                                    unsigned long long key);
 
-// Key (value, first column) of this thread's elements of vectors
-// [v_lo, v_hi) of one logits row.  Elements are visited in increasing column
-// order (batch, then vector i, then element), so a strict '>' keeps the
-// first occurrence.
-// Checked build: a NaN among the elements read raises PE_ERR_NAN in *err.
-template <int DT>
-__device__ __forceinline__ unsigned long long thread_key(const uint4* row, int v_lo, int v_hi,
-                                                         uint32_t* err) {
-  using E = Elem<DT>;
-  const int tid = threadIdx.x;
-  float m = 0.f;
-  int col = -1;
-#ifdef PE_CHECKED
-  bool nan = false;
-#endif
-  for (int base = v_lo; base < v_hi; base += kBatchVecs) {
-    if (base + tid >= v_hi) break;  // this thread has no vector here or later
-    uint4 x[kVecPerThread];
-#pragma unroll
-    for (int i = 0; i < kVecPerThread; ++i) {
-      const int v = base + i * kThreads + tid;
-      x[i] = v < v_hi ? __ldcs(row + v) : E::neg_inf();
-    }
-#ifdef PE_CHECKED
-#pragma unroll
-    for (int i = 0; i < kVecPerThread; ++i) nan |= E::has_nan(x[i]);
-#endif
-    float vm[kVecPerThread];
-#pragma unroll
-    for (int i = 0; i < kVecPerThread; ++i) vm[i] = E::vmax(x[i]);
-    float gm = vm[0];
-#pragma unroll
-    for (int i = 1; i < kVecPerThread; ++i) gm = fmaxf(gm, vm[i]);
-    if (col < 0 || gm > m) {
-      // locate the first vector, then the first element, holding gm
-      uint4 q = x[kVecPerThread - 1];
-      int vi = kVecPerThread - 1;
-#pragma unroll
-      for (int i = kVecPerThread - 2; i >= 0; --i)
-        if (vm[i] == gm) {
-          q = x[i];
-          vi = i;
-        }
-      m = gm;
-      col = (base + vi * kThreads + tid) * E::kPerVec + E::first_equal(q, gm);
-    }
-  }
-#ifdef PE_CHECKED
-  if (nan) atomicOr(err, PE_ERR_NAN);
-#else
-  (void)err;
-#endif
-  return col >= 0 ? make_key(m, (uint32_t)col) : 0ull;
-}
-
 template <int DT>
 __device__ __forceinline__ void argmax_unit(const StepParams& p, SharedState& sh, int u) {
   const int tid = threadIdx.x;
@@ -435,7 +339,7 @@ __device__ __forceinline__ void argmax_unit(const StepParams& p, SharedState& sh
   const int v_hi = rowp ? min(v_lo + p.chunk_vecs, p.nvec) : v_lo;  // bad index: nothing
   if (!rowp && c == 0 && tid == 0) atomicOr(p.err, PE_ERR_ROW_RANGE);
   const unsigned long long key =
-      thread_key<DT>(reinterpret_cast<const uint4*>(rowp), v_lo, v_hi, p.err);
+      thread_key<DT, kThreads>(reinterpret_cast<const uint4*>(rowp), v_lo, v_hi, p.err);
   finish_argmax_unit<DT>(p, sh, r, c, rowp, key);
 }
 
@@ -446,30 +350,10 @@ template <int DT>
 __device__ __forceinline__ void finish_argmax_unit(const StepParams& p, SharedState& sh, int r,
                                                    int c, const char* rowp,
                                                    unsigned long long key) {
-  using E = Elem<DT>;
   const int tid = threadIdx.x;
   // leftover elements past the last whole vector (last chunk, one thread)
   if (p.tail && rowp && c == p.C - 1 && tid == 0) {
-    const int c0 = p.nvec * E::kPerVec;
-    float tm = E::scalar(rowp, c0);
-    int tc = c0;
-#ifdef PE_CHECKED
-    bool nan = tm != tm;
-#endif
-    for (int e = 1; e < p.tail; ++e) {
-      const float x = E::scalar(rowp, c0 + e);
-#ifdef PE_CHECKED
-      nan |= x != x;
-#endif
-      if (x > tm) {
-        tm = x;
-        tc = c0 + e;
-      }
-    }
-#ifdef PE_CHECKED
-    if (nan) atomicOr(p.err, PE_ERR_NAN);
-#endif
-    const unsigned long long tk = make_key(tm, (uint32_t)tc);
+    const unsigned long long tk = tail_key<DT>(rowp, p.nvec, p.tail, p.err);
     key = tk > key ? tk : key;
   }
 
@@ -493,7 +377,7 @@ __device__ __forceinline__ void finish_argmax_unit(const StepParams& p, SharedSt
   }
   __syncthreads();
   const int last = sh.last;
-  if (last >= 0) request_epilogue(p, sh, last);
+  if (last >= 0) request_epilogue<kKeysInWorkspace>(p, sh, last);
 }
 
 // ------------------------------------------------------- early-exit units
@@ -519,7 +403,6 @@ __device__ __forceinline__ int settled(unsigned long long st, int Kp) {
 
 template <int DT>
 __device__ __forceinline__ void argmax_unit_early(const StepParams& p, SharedState& sh, int u) {
-  using E = Elem<DT>;
   const int tid = threadIdx.x;
   const int per_row = p.B * p.C;
   const int j = u / per_row;
@@ -531,28 +414,9 @@ __device__ __forceinline__ void argmax_unit_early(const StepParams& p, SharedSta
   const int v_lo = c * p.chunk_vecs;
   const int v_hi = min(v_lo + p.chunk_vecs, p.nvec);
   unsigned long long key =
-      thread_key<DT>(reinterpret_cast<const uint4*>(rowp), v_lo, v_hi, p.err);
+      thread_key<DT, kThreads>(reinterpret_cast<const uint4*>(rowp), v_lo, v_hi, p.err);
   if (p.tail && c == p.C - 1 && tid == 0) {  // leftover elements past the last vector
-    const int c0 = p.nvec * E::kPerVec;
-    float tm = E::scalar(rowp, c0);
-    int tc = c0;
-#ifdef PE_CHECKED
-    bool nan = tm != tm;
-#endif
-    for (int e = 1; e < p.tail; ++e) {
-      const float x = E::scalar(rowp, c0 + e);
-#ifdef PE_CHECKED
-      nan |= x != x;
-#endif
-      if (x > tm) {
-        tm = x;
-        tc = c0 + e;
-      }
-    }
-#ifdef PE_CHECKED
-    if (nan) atomicOr(p.err, PE_ERR_NAN);
-#endif
-    const unsigned long long tk = make_key(tm, (uint32_t)tc);
+    const unsigned long long tk = tail_key<DT>(rowp, p.nvec, p.tail, p.err);
     key = tk > key ? tk : key;
   }
   key = warp_max_key(key);
@@ -600,7 +464,7 @@ __device__ __forceinline__ void argmax_unit_early(const StepParams& p, SharedSta
   __syncthreads();
   const int due = sh.last;
   const int a = sh.first;
-  if (due >= 0) request_epilogue<true>(p, sh, due, a);
+  if (due >= 0) request_epilogue<kRowsSettled>(p, sh, due, a);
 }
 
 // ------------------------------------------------------------------ X tiles
@@ -903,6 +767,91 @@ __global__ void __launch_bounds__(kThreads, 4) step_kernel(const StepParams p) {
   if (BULK && threadIdx.x == 0) bulk_wait_all_visible();  // stores done before the CTA ends
 }
 
+// ------------------------------------------------------------ single pass
+// When every unit of a step fits one per co-resident CTA (few requests),
+// the launch is cooperative (all CTAs resident at once) and CTA u does unit
+// u and leaves: no work counter, no unit counts.  An argmax unit stores its
+// chunk key into its own slot (one relaxed 64-bit store; a chunk of the
+// fused step always holds an element, so its key is never zero); the CTA of
+// a request's last chunk then waits, bounded, for the request's other slots
+// (their CTAs are resident and never wait on anything), keeps each row's
+// maximum, clears the slots and takes the verdict.  Each chunk thus pays one
+// store instead of a key merge, a device-scope fence and a counting atomic
+// in series, and the verdict reads its keys from shared memory.
+constexpr unsigned long long kSlotWaitNs = 20000000ull;  // 20 ms: never expected
+
+template <int DT>
+__device__ __forceinline__ void single_pass_argmax_unit(const StepParams& p, SharedState& sh,
+                                                        int u) {
+  const int tid = threadIdx.x;
+  const int r = u / p.C;
+  const int c = u - r * p.C;
+  const char* rowp = static_cast<const char*>(p.logits) + (long long)r * p.row_bytes;
+  const int v_lo = c * p.chunk_vecs;
+  const int v_hi = min(v_lo + p.chunk_vecs, p.nvec);
+  unsigned long long key =
+      thread_key<DT, kThreads>(reinterpret_cast<const uint4*>(rowp), v_lo, v_hi, p.err);
+  if (p.tail && c == p.C - 1 && tid == 0) {
+    const unsigned long long tk = tail_key<DT>(rowp, p.nvec, p.tail, p.err);
+    key = tk > key ? tk : key;
+  }
+  key = warp_max_key(key);
+  if ((tid & 31) == 0) sh.red[tid >> 5] = key;
+  __syncthreads();
+  if (tid < 32) {
+    unsigned long long k = tid < kWarps ? sh.red[tid] : 0ull;
+    k = warp_max_key(k);
+    if (tid == 0) st_relaxed(p.slots + u, k);
+  }
+  const int nr = p.Kp + 1;
+  const int b = r / nr;
+  if (r - b * nr != p.Kp || c != p.C - 1) return;  // not the request's last chunk
+  // the request's drafts and positions, then its rows' keys from the slots
+  const int io = seg_begin(p, b);
+  const int vb = seg_begin(p, b + 1) - io - 1 - p.Kp;
+  if (tid < nr) {
+    sh.rowkey[tid] = 0ull;
+    if (tid < p.Kp) sh.tok[tid] = __ldg(p.in_tokens + io + vb + tid + 1);
+    sh.pos[tid] = __ldg(p.in_positions + io + vb + tid);
+  }
+  __syncthreads();
+  const int n = nr * p.C;
+  unsigned long long* slot = p.slots + (long long)b * n;
+  bool late = false;
+  for (int i = tid; i < n; i += kThreads) {
+    unsigned long long v = ld_relaxed(slot + i);
+    if (v == 0ull) {
+      const unsigned long long t0 = global_ns();
+      while (v == 0ull && global_ns() - t0 < kSlotWaitNs) v = ld_relaxed(slot + i);
+    }
+    if (v == 0ull) {
+      late = true;
+    } else {
+      if (key_col(v) >= (uint32_t)p.V) atomicOr(p.err, PE_ERR_WORKSPACE);  // not a key of this call
+      atomicMax(&sh.rowkey[i / p.C], v);
+    }
+    slot[i] = 0ull;  // clear for the next call
+  }
+  if (late) atomicOr(p.err, PE_ERR_TIMEOUT);
+  __syncthreads();
+  request_epilogue<kKeysInShared>(p, sh, b);
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 4) step_kernel_single(const StepParams p) {
+  __shared__ SharedState sh;
+  if (p.in_offsets && !offsets_valid(p.in_offsets, p.B, p.R, p.Kp + 1)) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(p.err, PE_ERR_OFFSETS);
+    return;  // every CTA sees the same offsets and leaves without writing
+  }
+  uint32_t phase = 0;  // (register copy tiles: unused)
+  const int u = blockIdx.x;  // one unit per CTA: argmax chunks, then copy tiles
+  if (u < p.n_arg_units)
+    single_pass_argmax_unit<DT>(p, sh, u);
+  else
+    copy_tile<false>(p, sh, u - p.n_arg_units, nullptr, phase);
+}
+
 // --------------------------------------------------- early-exit scheduling
 // Units are handed out in order (argmax units row-major, then copy tiles).
 // A CTA takes its next unit only when it is free (a unit handed out is a
@@ -1077,6 +1026,67 @@ void bind_workspace(pe::StepParams& p, void* ws, int rows, int B) {
   p.keys = reinterpret_cast<unsigned long long*>(base + L.key_off);
   p.rcount = reinterpret_cast<uint32_t*>(base + L.rcount_off);
   p.amax_ws = reinterpret_cast<int32_t*>(base + L.amax_off);
+  p.slots = reinterpret_cast<unsigned long long*>(base + L.slot_off);
+}
+
+// Single-pass plan: chunks such that the `rows` rows' argmax units fit the
+// `avail` CTAs left beside the copy tiles, as many as fit (one unit per
+// CTA); false when that would take longer chunks than four load batches
+// (the persistent queue then balances the work better).
+bool plan_single(pe::StepParams& p, int elt, int rows, int avail) {
+  if (rows <= 0 || avail < rows) return false;
+  const int epv = 16 / elt;
+  p.Rl = rows;
+  p.nvec = p.V / epv;
+  p.tail = p.V % epv;
+  if (p.nvec == 0) {
+    p.C = 1;
+    p.chunk_vecs = 0;
+  } else {
+    const int cmax = avail / rows;
+    int chunk = (p.nvec + cmax - 1) / cmax;
+    const int grain = chunk > pe::kBatchVecs ? pe::kBatchVecs : pe::kThreads;
+    chunk = (chunk + grain - 1) / grain * grain;
+    if (chunk > 4 * pe::kBatchVecs) return false;
+    p.chunk_vecs = chunk;
+    p.C = (p.nvec + chunk - 1) / chunk;
+  }
+  p.n_arg_units = rows * p.C;
+  return p.n_arg_units <= pe::kSinglePassSlots;
+}
+
+// CTAs of the single-pass kernel one SM holds at once (cached per device).
+template <int DT>
+int single_ctas_per_sm(int dev) {
+  static std::atomic<int> cache[64];
+  int n = cache[dev].load(std::memory_order_relaxed);
+  if (n) return n;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, pe::step_kernel_single<DT>,
+                                                    pe::kThreads, 0) != cudaSuccess || n < 1)
+    n = -1;
+  (void)cudaGetLastError();
+  cache[dev].store(n, std::memory_order_relaxed);
+  return n;
+}
+
+// Cooperative launch: the driver starts every CTA at once or fails the launch.
+template <int DT>
+int launch_single(const pe::StepParams& p, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeCooperative;
+  attr.val.cooperative = 1;
+  cfg.gridDim = dim3(p.n_units);
+  cfg.blockDim = dim3(pe::kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, pe::step_kernel_single<DT>, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return PE_ECUDA;
+  }
+  return pe_host::launch_status();
 }
 
 }  // namespace
@@ -1258,7 +1268,29 @@ int step_common(const pe_step_args* a, void* stream, bool early) {
     early = false;
     p.mask_unread = 1;
   }
+
   const int grid_max = dev.sm_count * tn.ctas_per_sm;
+  // Few requests: one unit per CTA in a single cooperative pass (register
+  // copy tiles, the default queue order)
+  if (!early && tn.single_pass > 0 && tn.variant != 2) {
+    int dev_id = 0;
+    if (cudaGetDevice(&dev_id) != cudaSuccess || dev_id < 0 || dev_id >= 64) return PE_ECUDA;
+    const int per_sm = a->logits_dtype == PE_BF16 ? single_ctas_per_sm<PE_BF16>(dev_id)
+                                                  : single_ctas_per_sm<PE_F32>(dev_id);
+    const long long cap = per_sm > 0 ? (long long)dev.sm_count * per_sm : 0;
+    pe::StepParams q = p;
+    q.rows_per_unit = tn.rows_per_unit;
+    q.rv = rows;
+    q.n_vtile = (q.rv + q.rows_per_unit - 1) / q.rows_per_unit;
+    q.n_copy_units = q.n_vtile + (q.T - q.rv + q.rows_per_unit - 1) / q.rows_per_unit;
+    if (cap > q.n_copy_units && plan_single(q, elt, rows, (int)(cap - q.n_copy_units))) {
+      q.n_units = q.n_arg_units + q.n_copy_units;
+      bind_workspace(q, a->workspace, rows, B);
+      cudaStream_t st = static_cast<cudaStream_t>(stream);
+      return a->logits_dtype == PE_BF16 ? launch_single<PE_BF16>(q, st)
+                                        : launch_single<PE_F32>(q, st);
+    }
+  }
   plan_argmax(p, elt, rows, grid_max, tn.chunk_batches);
   // bulk-copy tiles (variant 2; the early-exit kernel copies through
   // registers): as many rows per tile as the staging buffer holds

@@ -13,6 +13,7 @@
 //   [..]  uint64 key[rows]     running (value, column) maximum per logits row
 //   [..]  uint32 rcount[rows]  early exit: finished chunks per row
 //   [..]  int32  amax[rows]    early exit: argmax of each completed row
+//   [..]  uint64 slot[1024]    single pass: each argmax unit's chunk key
 //
 // Every field is zero between calls, so one workspace serves calls of any
 // size up to the one it was sized for: the full step clears a request's keys
@@ -20,7 +21,8 @@
 // bonus row is written, the early-exit step clears completed
 // rows as they complete and everything else (partly read rows, states, row
 // results) in its last CTA; the last CTA to leave clears the two scheduler
-// words.
+// words; in the single pass, the CTA that collects a request's chunk keys
+// clears their slots.
 #pragma once
 
 #include <stddef.h>
@@ -28,8 +30,10 @@
 
 namespace pe {
 
+constexpr int kSinglePassSlots = 1024;  // argmax units of a single-pass step, at most
+
 struct WorkspaceLayout {
-  size_t count_off, state_off, xfer_off, key_off, rcount_off, amax_off, bytes;
+  size_t count_off, state_off, xfer_off, key_off, rcount_off, amax_off, slot_off, bytes;
   WorkspaceLayout(int64_t rows, int64_t B) {
     count_off = 8;
     state_off = (count_off + 4 * (size_t)B + 7) & ~(size_t)7;
@@ -37,7 +41,8 @@ struct WorkspaceLayout {
     key_off = xfer_off + 8 * (size_t)B;
     rcount_off = key_off + 8 * (size_t)rows;
     amax_off = rcount_off + 4 * (size_t)rows;
-    bytes = (amax_off + 4 * (size_t)rows + 255) & ~(size_t)255;
+    slot_off = (amax_off + 4 * (size_t)rows + 7) & ~(size_t)7;
+    bytes = (slot_off + 8 * (size_t)kSinglePassSlots + 255) & ~(size_t)255;
   }
 };
 

@@ -53,7 +53,8 @@ def test_status_strings(lib):
 
 
 def test_workspace_bytes(lib):
-    assert lib.pe_workspace_bytes(0, 0) == 256
+    # scheduler words, then the 1024 chunk-key slots of the single pass
+    assert lib.pe_workspace_bytes(0, 0) == (8 + 8 * 1024 + 255) // 256 * 256
     n = lib.pe_workspace_bytes(2048, 256)
     assert n >= 8 + 4 * 256 + 8 * 2048 and n % 256 == 0
     assert lib.pe_workspace_bytes(-1, 3) == 0

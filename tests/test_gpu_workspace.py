@@ -43,8 +43,10 @@ def _greedy_offsets(rows, B):
     xfer = state + 8 * B
     key = xfer + 8 * B
     rcount = key + 8 * rows
+    amax = rcount + 4 * rows
+    slot = (amax + 4 * rows + 7) & ~7
     return {"sched": 0, "ctas_done": 4, "count": count, "state": state, "xfer": xfer,
-            "key": key, "rcount": rcount}
+            "key": key, "rcount": rcount, "slot": slot}
 
 
 def _poke(ws, offset, value, nbytes):
@@ -73,7 +75,10 @@ class tuned:
         _native.set_tuning(**self.kw)
 
     def __exit__(self, *exc):
-        _native.set_tuning(**self.before)
+        b = dict(self.before)
+        if b["early_full_read_mb"] == 0:
+            b["early_full_read_mb"] = -1
+        _native.set_tuning(**b)
 
 
 # B=8, K'=7, V=151936: 64 rows of about ten chunks each, so per-row and
@@ -96,12 +101,33 @@ def test_fused_step_detects_dirty_workspace(field, off, nbytes, value, variant):
     rows = w.B * (w.Kp + 1)
     ws = _native.new_workspace(rows, w.B)
     _poke(ws, _greedy_offsets(rows, w.B)[field] + off, value, nbytes)
-    with tuned(variant=variant):
+    with tuned(variant=variant, single_pass=-1):  # the persistent queue, which uses them
         got = _run(w, ws, early=False)
         assert got["err"] & _native.ERR_WORKSPACE, field
         ws.zero_()
         again = _run(w, ws, early=False)
     assert_same(again, ref, what="after re-zeroing (%s)" % field)
+    assert int(ws.count_nonzero()) == 0
+
+
+@pytest.mark.parametrize("slot", [0, 7, 63], ids=["first", "second", "later_request"])
+def test_single_pass_detects_a_dirty_slot(slot):
+    """A few requests run as a single pass: each argmax unit stores its chunk
+    key into its own slot and the request's last chunk collects them.  A slot
+    left holding a value no chunk of this step can store is either
+    overwritten by its chunk before the collector reads it (the outputs are
+    then exact) or read first and reported; it is never taken silently."""
+    w = wl.make_workload(SPEC, 44, device="cuda")
+    ref = oracle_of(w)
+    rows = w.B * (w.Kp + 1)
+    ws = _native.new_workspace(rows, w.B)
+    _poke(ws, _greedy_offsets(rows, w.B)["slot"] + 8 * slot, KEY, 8)
+    got = _run(w, ws, early=False)
+    if not got["err"] & _native.ERR_WORKSPACE:
+        assert_same(got, ref, what="dirty slot %d overwritten in time" % slot)
+    ws.zero_()
+    again = _run(w, ws, early=False)
+    assert_same(again, ref, what="after re-zeroing (slot %d)" % slot)
     assert int(ws.count_nonzero()) == 0
 
 
