@@ -323,6 +323,56 @@ __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedStat
   }
 }
 
+// ------------------------------------------------------------ key slots
+// In the single pass (below) chunk keys travel through slots instead of
+// per-row atomic maxima: each argmax unit u stores its chunk key into slot u
+// (one relaxed 64-bit store; a chunk without an element would store 1, which
+// no key equals), and the CTA of the request's last chunk collects them.
+// The slot is its own message, so the store needs no fence.
+constexpr unsigned long long kEmptyChunk = 1ull;
+constexpr unsigned long long kSlotWaitNs = 20000000ull;  // 20 ms: never expected
+
+__device__ __forceinline__ unsigned long long slot_value(unsigned long long key) {
+  return key ? key : kEmptyChunk;
+}
+
+// The collecting CTA of request b: the drafts and positions into sh.tok /
+// sh.pos, then every chunk slot of the request (waiting, bounded, for those
+// still in flight), each row's maximum into sh.rowkey; the slots are left
+// zero for the next call.
+__device__ __forceinline__ void collect_request_keys(const StepParams& p, SharedState& sh,
+                                                     int b) {
+  const int tid = threadIdx.x;
+  const int nr = p.Kp + 1;
+  const int io = seg_begin(p, b);
+  const int vb = seg_begin(p, b + 1) - io - 1 - p.Kp;
+  if (tid < nr) {
+    sh.rowkey[tid] = 0ull;
+    if (tid < p.Kp) sh.tok[tid] = __ldg(p.in_tokens + io + vb + tid + 1);
+    if (p.full) sh.pos[tid] = __ldg(p.in_positions + io + vb + tid);
+  }
+  __syncthreads();
+  const int n = nr * p.C;
+  unsigned long long* slot = p.slots + (long long)b * n;
+  bool late = false;
+  for (int i = tid; i < n; i += kThreads) {
+    unsigned long long v = ld_relaxed(slot + i);
+    if (v == 0ull) {
+      const unsigned long long t0 = global_ns();
+      while (v == 0ull && global_ns() - t0 < kSlotWaitNs) v = ld_relaxed(slot + i);
+    }
+    if (v == 0ull) {
+      late = true;
+    } else if (v != kEmptyChunk) {
+      if (key_col(v) >= (uint32_t)p.V) atomicOr(p.err, PE_ERR_WORKSPACE);  // not a key of this call
+      atomicMax(&sh.rowkey[i / p.C], v);
+    }
+    slot[i] = 0ull;  // clear for the next call
+  }
+  if (late) atomicOr(p.err, PE_ERR_TIMEOUT);
+  __syncthreads();
+}
+
 // ------------------------------------------------------------- argmax chunk
 template <int DT>
 __device__ __forceinline__ void finish_argmax_unit(const StepParams& p, SharedState& sh, int r,
@@ -771,15 +821,12 @@ __global__ void __launch_bounds__(kThreads, 4) step_kernel(const StepParams p) {
 // When every unit of a step fits one per co-resident CTA (few requests),
 // the launch is cooperative (all CTAs resident at once) and CTA u does unit
 // u and leaves: no work counter, no unit counts.  An argmax unit stores its
-// chunk key into its own slot (one relaxed 64-bit store; a chunk of the
-// fused step always holds an element, so its key is never zero); the CTA of
-// a request's last chunk then waits, bounded, for the request's other slots
-// (their CTAs are resident and never wait on anything), keeps each row's
-// maximum, clears the slots and takes the verdict.  Each chunk thus pays one
-// store instead of a key merge, a device-scope fence and a counting atomic
-// in series, and the verdict reads its keys from shared memory.
-constexpr unsigned long long kSlotWaitNs = 20000000ull;  // 20 ms: never expected
-
+// chunk key into its slot; the CTA of a request's last chunk then waits,
+// bounded, for the request's other slots (their CTAs are resident and never
+// wait on anything), keeps each row's maximum, clears the slots and takes
+// the verdict.  Each chunk pays one store instead of a key merge, a
+// device-scope fence and a counting atomic in series, and the verdict reads
+// its keys from shared memory.
 template <int DT>
 __device__ __forceinline__ void single_pass_argmax_unit(const StepParams& p, SharedState& sh,
                                                         int u) {
@@ -801,39 +848,12 @@ __device__ __forceinline__ void single_pass_argmax_unit(const StepParams& p, Sha
   if (tid < 32) {
     unsigned long long k = tid < kWarps ? sh.red[tid] : 0ull;
     k = warp_max_key(k);
-    if (tid == 0) st_relaxed(p.slots + u, k);
+    if (tid == 0) st_relaxed(p.slots + u, slot_value(k));
   }
   const int nr = p.Kp + 1;
   const int b = r / nr;
   if (r - b * nr != p.Kp || c != p.C - 1) return;  // not the request's last chunk
-  // the request's drafts and positions, then its rows' keys from the slots
-  const int io = seg_begin(p, b);
-  const int vb = seg_begin(p, b + 1) - io - 1 - p.Kp;
-  if (tid < nr) {
-    sh.rowkey[tid] = 0ull;
-    if (tid < p.Kp) sh.tok[tid] = __ldg(p.in_tokens + io + vb + tid + 1);
-    sh.pos[tid] = __ldg(p.in_positions + io + vb + tid);
-  }
-  __syncthreads();
-  const int n = nr * p.C;
-  unsigned long long* slot = p.slots + (long long)b * n;
-  bool late = false;
-  for (int i = tid; i < n; i += kThreads) {
-    unsigned long long v = ld_relaxed(slot + i);
-    if (v == 0ull) {
-      const unsigned long long t0 = global_ns();
-      while (v == 0ull && global_ns() - t0 < kSlotWaitNs) v = ld_relaxed(slot + i);
-    }
-    if (v == 0ull) {
-      late = true;
-    } else {
-      if (key_col(v) >= (uint32_t)p.V) atomicOr(p.err, PE_ERR_WORKSPACE);  // not a key of this call
-      atomicMax(&sh.rowkey[i / p.C], v);
-    }
-    slot[i] = 0ull;  // clear for the next call
-  }
-  if (late) atomicOr(p.err, PE_ERR_TIMEOUT);
-  __syncthreads();
+  collect_request_keys(p, sh, b);
   request_epilogue<kKeysInShared>(p, sh, b);
 }
 
@@ -1029,12 +1049,34 @@ void bind_workspace(pe::StepParams& p, void* ws, int rows, int B) {
   p.slots = reinterpret_cast<unsigned long long*>(base + L.slot_off);
 }
 
-// Single-pass plan: chunks such that the `rows` rows' argmax units fit the
-// `avail` CTAs left beside the copy tiles, as many as fit (one unit per
-// CTA); false when that would take longer chunks than four load batches
-// (the persistent queue then balances the work better).
-bool plan_single(pe::StepParams& p, int elt, int rows, int avail) {
-  if (rows <= 0 || avail < rows) return false;
+// Single-pass plan for `rows` logits rows and `cap` co-resident CTAs: copy
+// tiles of 4, 8 or 16 X rows and argmax chunks such that every unit has a
+// CTA of its own, choosing the tile size that leaves the most CTAs to the
+// logits (so the most chunks per row; ties to the smaller tiles).  Chunks
+// are whole vectors per thread and as equal as that allows, since nothing
+// rebalances a static assignment.  False when not even one chunk per row
+// fits beside the tiles, or when chunks would exceed eight load batches:
+// with that much work per CTA, SMs that hold one CTA more than others set
+// the end (measured: B=64 decode, whole-row chunks, 46.1 us against 43.8
+// on the persistent queue; B=48 even; B=32, two chunks a row, 22.7 against
+// 23.7 inside a CUDA graph).
+bool plan_single(pe::StepParams& p, int elt, int rows, long long cap) {
+  if (rows <= 0) return false;
+  int best_rpu = 0;
+  long long best_c = 0;
+  for (int rpu : {p.rows_per_unit, 8, 16}) {
+    if (rpu < p.rows_per_unit) continue;
+    const long long n_copy = (p.rv + rpu - 1) / rpu + (p.T - p.rv + rpu - 1) / rpu;
+    const long long c = (cap - n_copy) / rows;
+    if (c > best_c) {
+      best_c = c;
+      best_rpu = rpu;
+    }
+  }
+  if (best_c < 1) return false;
+  p.rows_per_unit = best_rpu;
+  p.n_vtile = (p.rv + best_rpu - 1) / best_rpu;
+  p.n_copy_units = p.n_vtile + (p.T - p.rv + best_rpu - 1) / best_rpu;
   const int epv = 16 / elt;
   p.Rl = rows;
   p.nvec = p.V / epv;
@@ -1043,13 +1085,11 @@ bool plan_single(pe::StepParams& p, int elt, int rows, int avail) {
     p.C = 1;
     p.chunk_vecs = 0;
   } else {
-    const int cmax = avail / rows;
-    int chunk = (p.nvec + cmax - 1) / cmax;
-    const int grain = chunk > pe::kBatchVecs ? pe::kBatchVecs : pe::kThreads;
-    chunk = (chunk + grain - 1) / grain * grain;
-    if (chunk > 4 * pe::kBatchVecs) return false;
-    p.chunk_vecs = chunk;
-    p.C = (p.nvec + chunk - 1) / chunk;
+    const long long per = (p.nvec + best_c - 1) / best_c;
+    const long long chunk = (per + pe::kThreads - 1) / pe::kThreads * pe::kThreads;
+    if (chunk > 8LL * pe::kBatchVecs) return false;
+    p.chunk_vecs = (int)chunk;
+    p.C = (int)((p.nvec + chunk - 1) / chunk);
   }
   p.n_arg_units = rows * p.C;
   return p.n_arg_units <= pe::kSinglePassSlots;
@@ -1281,9 +1321,7 @@ int step_common(const pe_step_args* a, void* stream, bool early) {
     pe::StepParams q = p;
     q.rows_per_unit = tn.rows_per_unit;
     q.rv = rows;
-    q.n_vtile = (q.rv + q.rows_per_unit - 1) / q.rows_per_unit;
-    q.n_copy_units = q.n_vtile + (q.T - q.rv + q.rows_per_unit - 1) / q.rows_per_unit;
-    if (cap > q.n_copy_units && plan_single(q, elt, rows, (int)(cap - q.n_copy_units))) {
+    if (plan_single(q, elt, rows, cap)) {
       q.n_units = q.n_arg_units + q.n_copy_units;
       bind_workspace(q, a->workspace, rows, B);
       cudaStream_t st = static_cast<cudaStream_t>(stream);
