@@ -170,9 +170,9 @@ inline int launch_status() {
 }
 
 // Dynamic shared memory above 48 KiB must be opted into once per kernel and
-// device (a host-side attribute; no synchronisation).  The kernel also asks
-// for the largest shared-memory carveout, so that the occupancy it was
-// sized for (several such CTAs per SM) is not cut by a larger L1.
+// device (a host-side attribute; no synchronisation).  The carveout is left
+// to the driver: asking for the largest shared-memory share measured slower
+// (the argmax loads land in L1, whose size bounds the bytes in flight).
 template <class K>
 bool allow_smem(K kernel, int bytes, std::atomic<unsigned long long>& done_mask) {
   int dev = 0;
@@ -180,9 +180,7 @@ bool allow_smem(K kernel, int bytes, std::atomic<unsigned long long>& done_mask)
   const unsigned long long bit = 1ull << dev;
   if (done_mask.load(std::memory_order_relaxed) & bit) return true;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
-          cudaSuccess ||
-      cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+      cudaSuccess)
     return false;
   done_mask.fetch_or(bit);
   return true;
