@@ -833,12 +833,13 @@ __device__ __forceinline__ void single_pass_argmax_unit(const StepParams& p, Sha
   const int tid = threadIdx.x;
   const int r = u / p.C;
   const int c = u - r * p.C;
-  const char* rowp = static_cast<const char*>(p.logits) + (long long)r * p.row_bytes;
+  const char* rowp = logits_row(p, r);
   const int v_lo = c * p.chunk_vecs;
-  const int v_hi = min(v_lo + p.chunk_vecs, p.nvec);
+  const int v_hi = rowp ? min(v_lo + p.chunk_vecs, p.nvec) : v_lo;  // bad index: nothing
+  if (!rowp && c == 0 && tid == 0) atomicOr(p.err, PE_ERR_ROW_RANGE);
   unsigned long long key =
       thread_key<DT, kThreads>(reinterpret_cast<const uint4*>(rowp), v_lo, v_hi, p.err);
-  if (p.tail && c == p.C - 1 && tid == 0) {
+  if (p.tail && rowp && c == p.C - 1 && tid == 0) {
     const unsigned long long tk = tail_key<DT>(rowp, p.nvec, p.tail, p.err);
     key = tk > key ? tk : key;
   }
@@ -1062,21 +1063,25 @@ void bind_workspace(pe::StepParams& p, void* ws, int rows, int B) {
 // 23.7 inside a CUDA graph).
 bool plan_single(pe::StepParams& p, int elt, int rows, long long cap) {
   if (rows <= 0) return false;
-  int best_rpu = 0;
+  int best_rpu = p.rows_per_unit;
   long long best_c = 0;
-  for (int rpu : {p.rows_per_unit, 8, 16}) {
-    if (rpu < p.rows_per_unit) continue;
-    const long long n_copy = (p.rv + rpu - 1) / rpu + (p.T - p.rv + rpu - 1) / rpu;
-    const long long c = (cap - n_copy) / rows;
-    if (c > best_c) {
-      best_c = c;
-      best_rpu = rpu;
+  if (!p.full) {  // verification or readout alone: argmax units only
+    best_c = cap / rows;
+  } else {
+    for (int rpu : {p.rows_per_unit, 8, 16}) {
+      if (rpu < p.rows_per_unit) continue;
+      const long long n_copy = (p.rv + rpu - 1) / rpu + (p.T - p.rv + rpu - 1) / rpu;
+      const long long c = (cap - n_copy) / rows;
+      if (c > best_c) {
+        best_c = c;
+        best_rpu = rpu;
+      }
     }
   }
   if (best_c < 1) return false;
   p.rows_per_unit = best_rpu;
-  p.n_vtile = (p.rv + best_rpu - 1) / best_rpu;
-  p.n_copy_units = p.n_vtile + (p.T - p.rv + best_rpu - 1) / best_rpu;
+  p.n_vtile = p.full ? (p.rv + best_rpu - 1) / best_rpu : 0;
+  p.n_copy_units = p.full ? p.n_vtile + (p.T - p.rv + best_rpu - 1) / best_rpu : 0;
   const int epv = 16 / elt;
   p.Rl = rows;
   p.nvec = p.V / epv;
@@ -1129,6 +1134,29 @@ int launch_single(const pe::StepParams& p, cudaStream_t stream) {
   return pe_host::launch_status();
 }
 
+constexpr int kNotTaken = 1;  // try_single: the step does not fit one pass
+
+// Few requests: plan, bind and launch the single pass when every unit fits
+// one per co-resident CTA (register copy tiles only); kNotTaken otherwise,
+// with nothing enqueued.  p holds the step's arguments, rows its logits
+// rows (verified rows for pe_step; rv, T and rows_per_unit set when it
+// copies).
+int try_single(const pe::StepParams& p_in, int dtype, int elt, int rows, int B, void* ws,
+               const pe_host::Tuning& tn, const pe_host::DeviceInfo& dev, void* stream) {
+  if (tn.single_pass <= 0 || tn.variant == 2) return kNotTaken;
+  int dev_id = 0;
+  if (cudaGetDevice(&dev_id) != cudaSuccess || dev_id < 0 || dev_id >= 64) return PE_ECUDA;
+  const int per_sm = dtype == PE_BF16 ? single_ctas_per_sm<PE_BF16>(dev_id)
+                                      : single_ctas_per_sm<PE_F32>(dev_id);
+  const long long cap = per_sm > 0 ? (long long)dev.sm_count * per_sm : 0;
+  pe::StepParams q = p_in;
+  if (!plan_single(q, elt, rows, cap)) return kNotTaken;
+  q.n_units = q.n_arg_units + q.n_copy_units;
+  bind_workspace(q, ws, rows, B);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  return dtype == PE_BF16 ? launch_single<PE_BF16>(q, st) : launch_single<PE_F32>(q, st);
+}
+
 }  // namespace
 
 extern "C" {
@@ -1166,6 +1194,8 @@ int pe_verify_greedy(const void* logits, int dtype, int64_t row_stride, int32_t 
   p.target_argmax = target_argmax;
   p.err = err;
   const int rows = B * (Kp + 1);
+  const int single = try_single(p, dtype, elt, rows, B, workspace, tn, dev, stream);
+  if (single != kNotTaken) return single;
   const int grid_max = dev.sm_count * tn.ctas_per_sm;
   plan_argmax(p, elt, rows, grid_max, tn.chunk_batches);
   p.n_units = p.n_arg_units;
@@ -1203,6 +1233,8 @@ int pe_draft_readout(const void* logits, int dtype, int64_t row_stride, int32_t 
   p.rows_total = rows;
   p.bonus_token = out_tokens;
   p.err = err;
+  const int single = try_single(p, dtype, elt, n, n, workspace, tn, dev, stream);
+  if (single != kNotTaken) return single;
   const int grid_max = dev.sm_count * tn.ctas_per_sm;
   plan_argmax(p, elt, n, grid_max, tn.chunk_batches);
   p.n_units = p.n_arg_units;
@@ -1310,24 +1342,13 @@ int step_common(const pe_step_args* a, void* stream, bool early) {
   }
 
   const int grid_max = dev.sm_count * tn.ctas_per_sm;
-  // Few requests: one unit per CTA in a single cooperative pass (register
-  // copy tiles, the default queue order)
-  if (!early && tn.single_pass > 0 && tn.variant != 2) {
-    int dev_id = 0;
-    if (cudaGetDevice(&dev_id) != cudaSuccess || dev_id < 0 || dev_id >= 64) return PE_ECUDA;
-    const int per_sm = a->logits_dtype == PE_BF16 ? single_ctas_per_sm<PE_BF16>(dev_id)
-                                                  : single_ctas_per_sm<PE_F32>(dev_id);
-    const long long cap = per_sm > 0 ? (long long)dev.sm_count * per_sm : 0;
+  // Few requests: one unit per CTA in a single cooperative pass
+  if (!early) {
     pe::StepParams q = p;
     q.rows_per_unit = tn.rows_per_unit;
     q.rv = rows;
-    if (plan_single(q, elt, rows, cap)) {
-      q.n_units = q.n_arg_units + q.n_copy_units;
-      bind_workspace(q, a->workspace, rows, B);
-      cudaStream_t st = static_cast<cudaStream_t>(stream);
-      return a->logits_dtype == PE_BF16 ? launch_single<PE_BF16>(q, st)
-                                        : launch_single<PE_F32>(q, st);
-    }
+    const int single = try_single(q, a->logits_dtype, elt, rows, B, a->workspace, tn, dev, stream);
+    if (single != kNotTaken) return single;
   }
   plan_argmax(p, elt, rows, grid_max, tn.chunk_batches);
   // bulk-copy tiles (variant 2; the early-exit kernel copies through

@@ -4,7 +4,8 @@ the CPU oracle.
 Each case draws the batch (requests, draft depths, vocabulary, hidden size,
 element type, prompt lengths for the first step after prefill, accept-length
 distribution) and the launch-shape knobs (CTAs per SM, chunk size, copy-tile
-rows, kernel variant, queue order) from one seed, so that the combinations
+rows, kernel variant, queue order, single pass) from one seed, so that the
+combinations
 the fixed tests do not name (tiles straddling requests, tiny vocabularies,
 one-row prompts, K = 1, both sides of the bonus-row hand-off) are covered.
 Every output is compared bit for bit; the workspace must be left zeroed."""
@@ -57,7 +58,8 @@ def _spec(rng: random.Random, i: int) -> wl.WorkloadSpec:
 def _tuning(rng: random.Random) -> dict:
     return dict(ctas_per_sm=rng.choice([1, 2, 4]), chunk_batches=rng.choice([1, 2, 3, 4]),
                 rows_per_unit=rng.choice([1, 2, 3, 4, 8, 16]), variant=rng.choice([1, 1, 2]),
-                queue_order=rng.choice([1, 2]), early_full_read_mb=rng.choice([-1, 128]))
+                queue_order=rng.choice([1, 2]), early_full_read_mb=rng.choice([-1, 128]),
+                single_pass=rng.choice([1, -1]))
 
 
 def _run_early(w):

@@ -152,6 +152,11 @@ def test_early_exit_detects_dirty_workspace(field, off, nbytes, value):
 
 
 def test_verify_and_readout_detect_dirty_workspace():
+    with tuned(single_pass=-1):  # the persistent queue, which uses these words
+        _verify_and_readout_detect_dirty_workspace()
+
+
+def _verify_and_readout_detect_dirty_workspace():
     w = wl.make_workload(SPEC, 43, device="cuda")
     rows = w.B * (w.Kp + 1)
     ref = oracle.argmax_rows(w.logits.cpu())
