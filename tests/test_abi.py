@@ -175,6 +175,20 @@ def test_tuning_roundtrip(lib):
         assert _native.get_tuning()["early_full_read_mb"] == 0
         with pytest.raises(_native.PEError):
             _native.set_tuning(early_full_read_mb=-2)
+        _native.set_tuning(single_pass=-1)
+        assert _native.get_tuning()["single_pass"] == -1
+        _native.set_tuning(single_pass=1)
+        assert _native.get_tuning()["single_pass"] == 1
+        with pytest.raises(_native.PEError):
+            _native.set_tuning(single_pass=2)
     finally:
         _native.set_tuning(**{k: (v if v or k != "early_full_read_mb" else -1)
                               for k, v in before.items()})
+
+
+def test_latency_floor_rejects(lib):
+    s = ctypes.c_void_p(0)
+    assert lib.pe_latency_floor(0, 0, None, 0, None, s) == -1           # no CTA
+    assert lib.pe_latency_floor(4, -1, None, 0, None, s) == -1          # negative hops
+    assert lib.pe_latency_floor(4, 1, None, 1, ctypes.c_void_p(FAKE), s) == -1  # no chain
+    assert lib.pe_latency_floor(4, 1, ctypes.c_void_p(FAKE), 0, ctypes.c_void_p(FAKE), s) == -1
