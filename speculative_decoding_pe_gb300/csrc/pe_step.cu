@@ -1114,7 +1114,12 @@ int single_ctas_per_sm(int dev) {
   return n;
 }
 
-// Cooperative launch: the driver starts every CTA at once or fails the launch.
+constexpr int kNotTaken = 1;  // try_single: the step does not run as one pass
+
+// Cooperative launch: the driver starts every CTA at once or refuses the
+// launch (for instance while other work holds part of the GPU); a refusal
+// leaves no error behind and returns kNotTaken, so the caller runs the
+// persistent queue instead.
 template <int DT>
 int launch_single(const pe::StepParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg = {};
@@ -1129,16 +1134,14 @@ int launch_single(const pe::StepParams& p, cudaStream_t stream) {
   cfg.numAttrs = 1;
   if (cudaLaunchKernelEx(&cfg, pe::step_kernel_single<DT>, p) != cudaSuccess) {
     (void)cudaGetLastError();
-    return PE_ECUDA;
+    return kNotTaken;
   }
   return pe_host::launch_status();
 }
 
-constexpr int kNotTaken = 1;  // try_single: the step does not fit one pass
-
 // Few requests: plan, bind and launch the single pass when every unit fits
-// one per co-resident CTA (register copy tiles only); kNotTaken otherwise,
-// with nothing enqueued.  p holds the step's arguments, rows its logits
+// one per co-resident CTA (register copy tiles only); kNotTaken otherwise
+// (or when the cooperative launch is refused), with nothing enqueued.  p holds the step's arguments, rows its logits
 // rows (verified rows for pe_step; rv, T and rows_per_unit set when it
 // copies).
 int try_single(const pe::StepParams& p_in, int dtype, int elt, int rows, int B, void* ws,
