@@ -834,7 +834,7 @@ int pe_verify_sampled(const void* target_logits, const void* draft_logits, int d
   p.rlist = reinterpret_cast<int32_t*>(w + L.rlist_off);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // persistent grids: 3 CTAs (24 warps) per SM, fewer for small problems
+  // persistent grids: kStatsCtasPerSm CTAs (32 warps) per SM, fewer for small problems
   const long long n1 = ceil_div(rows * p.C, pe::kWarps);
   const int g1_max = dev.sm_count * pe::kStatsCtasPerSm;
   const int g1 = n1 < g1_max ? (int)n1 : g1_max;
