@@ -322,8 +322,8 @@ int pe_step_early_exit(const pe_step_args* args /* host */, void* stream);
  * NULL).  The scratch is a fixed array of PE_NOALLOC_WS_BYTES bytes inside
  * the library, held by every GPU that loads it until the process exits.
  *  - The first call on a device looks up the array's device address (and
- *    may load the library's GPU code there): make that first call before
- *    any stream capture.  The address is kept for the life of the process;
+ *    may load the library's GPU code there).  The address is kept for the
+ *    life of the process;
  *    a program that resets a device (cudaDeviceReset) must not call this
  *    entry point on that device afterwards (the kept address would no
  *    longer be the array's).
