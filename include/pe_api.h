@@ -73,9 +73,10 @@ typedef enum pe_dtype { PE_F32 = 0, PE_BF16 = 1 } pe_dtype;
 #define PE_ERR_MAP_RANGE 16u  /* hidden_map entry outside [0,T): skipped    */
 #define PE_ERR_ROW_RANGE 64u  /* readout row index outside [0,rows): -1     */
 #define PE_ERR_TIMEOUT 32u    /* a bounded wait gave up (a bulk-copy tile
-                                 waiting for its own loads, the sampled
-                                 stats merge); outputs incomplete; never
-                                 expected with a zeroed workspace          */
+                                 waiting for its own loads, the single
+                                 pass's collection of its chunk keys, the
+                                 sampled stats merge); outputs incomplete;
+                                 never expected with a zeroed workspace    */
 /* Raised only by the checked build (libpe_checked.so: the same entry points
  * compiled with PE_CHECKED, for debugging; slower).  Neither traps. */
 #define PE_ERR_NAN 128u       /* a logits row read by the greedy argmax
@@ -125,7 +126,9 @@ size_t pe_workspace_bytes(int32_t logits_rows, int32_t B);
  *  bonus_token [B] out: argmax of row a_b (the target's own next token).
  *  target_argmax [B*(Kp+1)] out, or NULL: every row's argmax.
  *  workspace   pe_workspace_bytes(B*(Kp+1), B) bytes, zeroed (see above).
- *  err         device error word (PE_ERR_WORKSPACE only).
+ *  err         device error word: PE_ERR_WORKSPACE; PE_ERR_TIMEOUT (the
+ *              single pass's bounded wait, never expected); PE_ERR_NAN in
+ *              the checked build.
  * B == 0 enqueues nothing. */
 int pe_verify_greedy(const void* logits, int dtype, int64_t row_stride,
                      int32_t B, int32_t Kp, int32_t V, const int32_t* in_tokens,
