@@ -1053,9 +1053,10 @@ void bind_workspace(pe::StepParams& p, void* ws, int rows, int B) {
 // Single-pass plan for `rows` logits rows and `cap` co-resident CTAs: copy
 // tiles of 4, 8 or 16 X rows and argmax chunks such that every unit has a
 // CTA of its own, choosing the tile size that leaves the most CTAs to the
-// logits (so the most chunks per row; ties to the smaller tiles).  Chunks
-// are whole vectors per thread and as equal as that allows, since nothing
-// rebalances a static assignment.  False when not even one chunk per row
+// logits (so the most chunks per row; ties to the smaller tiles), with no
+// chunk below half a load batch per thread.  Chunks are whole vectors per
+// thread and as equal as that allows, since nothing rebalances a static
+// assignment.  False when not even one chunk per row
 // fits beside the tiles, or when chunks would exceed eight load batches:
 // with that much work per CTA, SMs that hold one CTA more than others set
 // the end (measured: B=64 decode, whole-row chunks, 46.1 us against 43.8
@@ -1078,6 +1079,14 @@ bool plan_single(pe::StepParams& p, int elt, int rows, long long cap) {
       }
     }
   }
+  // Chunks of at least half a load batch per thread: measured faster than
+  // more, thinner ones (B=1 decode, V=201088: 200 chunks of 4 vectors a
+  // thread 10.7 us launched / 6.1 in a CUDA graph, against 400 chunks of 2
+  // vectors 12.2 / 6.8; 104 chunks of 8 vectors 10.7 / 6.1).
+  const long long nv = p.V / (16 / elt);
+  const long long min_chunk = (long long)(pe::kVecPerThread / 2) * pe::kThreads;
+  const long long c_cap = (nv + min_chunk - 1) / min_chunk;
+  if (c_cap >= 1 && best_c > c_cap) best_c = c_cap;
   if (best_c < 1) return false;
   p.rows_per_unit = best_rpu;
   p.n_vtile = p.full ? (p.rv + best_rpu - 1) / best_rpu : 0;
