@@ -1150,9 +1150,9 @@ int launch_single(const pe::StepParams& p, cudaStream_t stream) {
 
 // Few requests: plan, bind and launch the single pass when every unit fits
 // one per co-resident CTA (register copy tiles only); kNotTaken otherwise
-// (or when the cooperative launch is refused), with nothing enqueued.  p holds the step's arguments, rows its logits
-// rows (verified rows for pe_step; rv, T and rows_per_unit set when it
-// copies).
+// (or when the cooperative launch is refused), with nothing enqueued.
+// p holds the step's arguments, rows its logits rows (verified rows for
+// pe_step; rv, T and rows_per_unit set when it copies).
 int try_single(const pe::StepParams& p_in, int dtype, int elt, int rows, int B, void* ws,
                const pe_host::Tuning& tn, const pe_host::DeviceInfo& dev, void* stream) {
   if (tn.single_pass <= 0 || tn.variant == 2) return kNotTaken;
