@@ -272,14 +272,16 @@ namespace pe {
 // y = logit * c2, and, for the bonus row (DRAW), into the lane's best Gumbel
 // score y + G log2(e), pruned by the bound above against the best score of
 // the warp (shared after every batch).  Vectors past the chunk read as -inf
-// and contribute nothing.  The bonus row takes half the vectors per batch:
-// the noise needs the registers.
+// and contribute nothing.  The bonus row takes a quarter of the vectors per
+// batch: the noise needs the registers, and with half of them the kernel
+// spilled at its 64 registers (248.5 us per B=256 call against 241.2
+// without the spill).
 template <int DT, bool DRAW>
 __device__ __forceinline__ void fold_chunk(const SampledParams& p, const char* rowp, int v_lo,
                                            int v_hi, int b, int lane, float& m, float& s,
                                            Best& best) {
   using E = Vec<DT>;
-  constexpr int kV = DRAW ? kVecPerThread / 2 : kVecPerThread;
+  constexpr int kV = DRAW ? kVecPerThread / 4 : kVecPerThread;
   const uint4* row = reinterpret_cast<const uint4*>(rowp);
   const uint4 neg = make_uint4(E::kNegInf, E::kNegInf, E::kNegInf, E::kNegInf);
   float thr = -INFINITY;
@@ -590,7 +592,9 @@ __device__ __forceinline__ void residual_unit(const SampledParams& p, int u, int
     const uint4* dr = reinterpret_cast<const uint4*>(drow);
     const int v_lo = c * p.chunk2_vecs;
     const int v_hi = min(v_lo + p.chunk2_vecs, p.nvec);
-    constexpr int kV = kVecPerThread / 4;  // two rows, and registers for the noise
+    // one vector of each row per batch: with two the kernel spilled at its
+    // 64 registers (241.2 us per B=256 call against 239.3 without)
+    constexpr int kV = kVecPerThread / 8;
     float thr = -INFINITY;  // best score of the warp so far (absolute log2 units)
     for (int base = v_lo; base < v_hi; base += 32 * kV) {
       const float K = ex2(thr) * kBound;  // d > K t: the column may beat thr
