@@ -277,3 +277,22 @@ def test_sampled_argument_errors():
                                acc, bon, ws, err)
     torch.cuda.synchronize()
     assert int(ws.count_nonzero()) == 0
+
+
+# Seeded random shapes: batch, draft depth (0 included), vocabulary (ragged
+# tails, below one vector, many chunks), element type and temperature all
+# drawn from one generator per case.
+@pytest.mark.parametrize("case", range(24))
+def test_sampled_fuzz(case):
+    rng = np.random.default_rng(4242 + case)
+    B = int(rng.integers(1, 33))
+    Kp = int(rng.integers(0, 9))
+    V = int(rng.choice([int(rng.integers(1, 9)), int(rng.integers(9, 3000)),
+                        int(rng.integers(3000, 70001))]))
+    dtype = torch.bfloat16 if rng.random() < 0.7 else torch.float32
+    T = float(rng.choice([0.3, 0.7, 1.0, 1.6, 3.0]))
+    s = wl.make_sampled_inputs(B, Kp, V, dtype=dtype, seed=3000 + case)
+    seed = int(rng.integers(0, 2**63))
+    ref = run_oracle(s, T, seed)
+    got = run_gpu(s, T, seed)
+    assert_parity(s, T, seed, got, ref)
