@@ -56,3 +56,41 @@ def test_steps_captured_in_one_graph(name, early_exit):
             keys = [k for k in harness.OUTPUT_KEYS if not (early_exit and k == "target_argmax")]
             assert_same(got, ref, keys=keys + ["err"], what=name)
         assert int(ws.count_nonzero()) == 0
+
+
+def test_sampled_verification_captured_in_one_graph():
+    """pe_verify_sampled (a stats launch, then the residual launch as its
+    programmatic dependent) captured twice with distinct inputs and one
+    workspace; every replay equals the same calls made eagerly."""
+    cases = [wl.make_sampled_inputs(24, 5, 20011, seed=60 + i).to("cuda") for i in range(2)]
+    ws = torch.zeros(_native.workspace_bytes_sampled(24, 5), dtype=torch.uint8, device="cuda")
+    outs = [(torch.empty(24, dtype=torch.int32, device="cuda"),
+             torch.empty(24, dtype=torch.int32, device="cuda"), _native.new_error_word())
+            for _ in cases]
+
+    def call(i, stream):
+        s, (acc, bon, err) = cases[i], outs[i]
+        _native.verify_sampled(s.target_logits, s.draft_logits, s.Kp, s.tokens, s.u_accept,
+                               0.9, 77 + i, acc, bon, ws, err, stream)
+
+    for i in range(2):  # eager results (and the first call on the device)
+        call(i, None)
+    torch.cuda.synchronize()
+    ref = [(a.clone(), b.clone()) for a, b, _ in outs]
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        for i in range(2):
+            call(i, torch.cuda.current_stream())
+    for _ in range(2):
+        for acc, bon, err in outs:
+            acc.fill_(-5)
+            bon.fill_(-5)
+            err.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        for (acc, bon, err), (ra, rb) in zip(outs, ref):
+            assert int(err.item()) == 0
+            assert torch.equal(acc, ra) and torch.equal(bon, rb)
+        assert int(ws.count_nonzero()) == 0
