@@ -439,8 +439,11 @@ __device__ __forceinline__ void finish_argmax_unit(const StepParams& p, SharedSt
 // ORs two bits into the request's state word (row done; row's argmax equals
 // the draft).  The OR after which the rows 0..a are all done, 0..a-1 all
 // match and a mismatches (or a = K') settles the request: exactly one CTA
-// sees that change, and it runs the epilogue.  Nothing ever waits for
-// another CTA.
+// sees that change, and it runs the epilogue.  A chunk that ends before its
+// row completes ORs bit j into the request's count word when its key beats
+// the draft's own key (the row's argmax cannot be the draft), so the later
+// rows turn moot without waiting for the whole row (B=256 61.1 us against
+// 62.5, B=64 37.5 against 39.1).  Nothing ever waits for another CTA.
 
 // Accepted length settled by a state word, or -1 while it is still open.
 __device__ __forceinline__ int settled(unsigned long long st, int Kp) {
@@ -463,8 +466,16 @@ __device__ __forceinline__ void argmax_unit_early(const StepParams& p, SharedSta
   const char* rowp = logits_row(p, r);
   const int v_lo = c * p.chunk_vecs;
   const int v_hi = min(v_lo + p.chunk_vecs, p.nvec);
+  int d = -1;  // the draft this row is compared with (thread 0; loaded while the chunk streams)
+  if (tid == 0 && j < p.Kp) {
+    const int io = seg_begin(p, b);
+    const int vb = seg_begin(p, b + 1) - io - 1 - p.Kp;
+    d = __ldg(p.in_tokens + io + vb + j + 1);
+  }
   unsigned long long key =
       thread_key<DT, kThreads>(reinterpret_cast<const uint4*>(rowp), v_lo, v_hi, p.err);
+  float xd = 0.f;  // the draft's own logit
+  if (tid == 0 && d >= 0 && d < p.V) xd = Elem<DT>::scalar(rowp, d);
   if (p.tail && c == p.C - 1 && tid == 0) {  // leftover elements past the last vector
     const unsigned long long tk = tail_key<DT>(rowp, p.nvec, p.tail, p.err);
     key = tk > key ? tk : key;
@@ -481,6 +492,12 @@ __device__ __forceinline__ void argmax_unit_early(const StepParams& p, SharedSta
       fence_acq_rel();  // release
       const unsigned rc = atomicAdd(p.rcount + r, 1u);
       if (rc >= (unsigned)p.C) atomicOr(p.err, PE_ERR_WORKSPACE);  // did not start at zero
+      // A chunk whose key beats the draft's own key proves the row's argmax
+      // is not the draft: the request mismatches at row j at the latest, so
+      // its later rows are moot before the row completes.
+      if (j < p.Kp && rc < (unsigned)(p.C - 1) &&
+          (d < 0 || d >= p.V || k > make_key(xd, (uint32_t)d)))
+        atomicOr(p.count + b, 1u << j);
       if (rc == (unsigned)(p.C - 1)) {  // row r complete
         const unsigned long long kk = atomicExch(p.keys + r, 0ull);
         atomicExch(p.rcount + r, 0u);
@@ -901,8 +918,9 @@ __device__ __forceinline__ int skip_moot(const StepParams& p, unsigned q) {
     if (j == 0) return u;
     const int b = (u - j * per_row) / p.C;
     const unsigned long long st = __ldcg(p.state + b);
+    const unsigned early = __ldcg(p.count + b);  // mismatches found before their row completed
     const unsigned done = (unsigned)st, match = (unsigned)(st >> 32);
-    if (!(done & ~match & ((1u << j) - 1u))) return u;  // no earlier mismatch known
+    if (!(((done & ~match) | early) & ((1u << j) - 1u))) return u;  // no earlier mismatch known
     q = claim_early(p);                                 // moot: take the next one
   }
   return p.n_units;
@@ -945,7 +963,9 @@ __global__ void __launch_bounds__(kThreads, 4) step_kernel_early(const StepParam
     // first mismatch); one that has not lost units to a dirty counter
     for (int i = threadIdx.x; i < p.B; i += kThreads) {
       if (settled(p.state[i], p.Kp) < 0) atomicOr(p.err, PE_ERR_WORKSPACE);
+      if (p.Kp < 32 && (p.count[i] >> p.Kp)) atomicOr(p.err, PE_ERR_WORKSPACE);
       p.state[i] = 0ull;
+      p.count[i] = 0u;
     }
     if (threadIdx.x == 0) {
       atomicExch(p.sched, 0u);

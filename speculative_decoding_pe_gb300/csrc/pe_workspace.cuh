@@ -2,7 +2,8 @@
 //
 //   [0]   uint32 next_unit     dynamic work counter of the persistent grid
 //   [4]   uint32 ctas_done     CTAs that have left the work loop
-//   [8]   uint32 count[B]      finished argmax units per request
+//   [8]   uint32 count[B]      finished argmax units per request (early exit:
+//                              rows known to mismatch before they complete)
 //   [..]  uint64 state[B]      early exit: rows done (bits 0-31) and rows
 //                              whose argmax matched the draft (bits 32-63)
 //   [..]  uint64 xfer[B]       bonus-row hand-off between the copy tiles and
@@ -19,8 +20,8 @@
 // size up to the one it was sized for: the full step clears a request's keys
 // and count when its last unit arrives, and its hand-off word when the
 // bonus row is written, the early-exit step clears completed
-// rows as they complete and everything else (partly read rows, states, row
-// results) in its last CTA; the last CTA to leave clears the two scheduler
+// rows as they complete and everything else (partly read rows, states,
+// early-mismatch words, row results) in its last CTA; the last CTA to leave clears the two scheduler
 // words; in the single pass, the CTA that collects a request's chunk keys
 // clears their slots.
 #pragma once

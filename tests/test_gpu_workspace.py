@@ -90,7 +90,8 @@ SPEC = wl.SPECS["decode_b256"].with_(B=8, H=256, bt_width=4097)
 FULL_CASES = [("sched", 0, 4, U32), ("count", 4, 4, U32), ("xfer", 8, 8, U64),
               ("key", 8 * 8, 8, KEY)]
 EARLY_CASES = [("sched", 0, 4, U32), ("ctas_done", 0, 4, U32), ("state", 8, 8, U64),
-               ("rcount", 4 * 8, 4, U32), ("key", 8 * 8, 8, KEY), ("xfer", 8, 8, U64)]
+               ("rcount", 4 * 8, 4, U32), ("key", 8 * 8, 8, KEY), ("xfer", 8, 8, U64),
+               ("count", 4, 4, U32)]  # early exit: request 1's early-mismatch word
 
 
 @pytest.mark.parametrize("variant", [1, 2], ids=["regs", "bulk"])
