@@ -266,8 +266,8 @@ __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedStat
   }
   unsigned long long old = 0ull;
   if (tid == 0)
-    old = atomicOr(p.xfer + b, kXferVerdict | ((unsigned long long)a << 17) |
-                                   ((unsigned long long)(uint32_t)bonus << 32));
+    old = atom_or_acquire(p.xfer + b, kXferVerdict | ((unsigned long long)a << 17) |
+                                          ((unsigned long long)(uint32_t)bonus << 32));
   // the bonus row's first 2*kThreads vectors, read now in case this verdict
   // is the one to write it (the embedding table never changes)
   const bool bok = bonus >= 0 && bonus < p.V;
@@ -307,10 +307,9 @@ __device__ __forceinline__ void request_epilogue(const StepParams& p, SharedStat
     const bool legal = xfer_legal(old, Kp, false);
     if (!legal) atomicOr(p.err, PE_ERR_WORKSPACE);
     const bool mine = legal && (old & kXferCount) == (unsigned long long)nr;
-    if (mine) {
-      atomicExch(p.xfer + b, 0ull);  // both sides are done: clear for the next call
-      fence_acq_rel();  // acquire: the tiles' writes of the row come before ours
-    }
+    // both sides are done: clear for the next call (the acquire above
+    // already orders the tiles' writes of the row before ours)
+    if (mine) st_relaxed(p.xfer + b, 0ull);
     sh.xwrite = mine ? 1 : 0;
   }
   __syncthreads();
@@ -741,14 +740,12 @@ __device__ __forceinline__ void copy_handoff(const StepParams& p, SharedState& s
   __syncthreads();
   if (tid < nrows && sh.vreq[tid] >= 0) {
     const int b = sh.vreq[tid];
-    fence_acq_rel();  // release
-    const unsigned long long old = atomicAdd(p.xfer + b, 1ull);
+    const unsigned long long old = atom_add_acq_rel(p.xfer + b, 1ull);
     if (!xfer_legal(old, p.Kp, true)) {
       atomicOr(p.err, PE_ERR_WORKSPACE);
     } else if ((old & kXferCount) + 1 == (unsigned long long)(p.Kp + 1) &&
                (old & kXferVerdict)) {
-      atomicExch(p.xfer + b, 0ull);  // both sides are done: clear for the next call
-      fence_acq_rel();  // acquire: other tiles' writes of the row come first
+      st_relaxed(p.xfer + b, 0ull);  // both sides are done: clear for the next call
       const int e = atomicAdd(&sh.nbonus, 1);
       sh.brow[e] = sh.vrow0[tid] + (int)((old >> 17) & 0xffull);
       sh.btok[e] = (int)(uint32_t)(old >> 32);
