@@ -79,6 +79,20 @@ __device__ __forceinline__ unsigned long long atom_add_acq_rel(unsigned long lon
                : "=l"(old) : "l"(a), "l"(v) : "memory");
   return old;
 }
+// Counting with release and acquire semantics in the atomic itself: each
+// arrival publishes what it wrote before (its key merge, a row's argmax),
+// and the arrival that completes the count acquires every other's, with no
+// fence on either side.
+__device__ __forceinline__ unsigned atom_add_acq_rel_u32(unsigned* a, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(a), "r"(v) : "memory");
+  return old;
+}
+__device__ __forceinline__ unsigned long long atom_or_acq_rel(unsigned long long* a, unsigned long long v) {
+  unsigned long long old;
+  asm volatile("atom.acq_rel.gpu.global.or.b64 %0, [%1], %2;" : "=l"(old) : "l"(a), "l"(v) : "memory");
+  return old;
+}
 __device__ __forceinline__ unsigned long long ld_relaxed(const unsigned long long* a) {
   unsigned long long v;
   asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(a) : "memory");

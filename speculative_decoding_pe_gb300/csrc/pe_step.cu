@@ -414,13 +414,13 @@ __device__ __forceinline__ void finish_argmax_unit(const StepParams& p, SharedSt
     k = warp_max_key(k);
     if (tid == 0) {
       atomicMax(p.keys + r, k);
-      fence_acq_rel();  // release
       const int b = r / (p.Kp + 1);
       const unsigned total = (unsigned)((p.Kp + 1) * p.C);
-      const unsigned done = atomicAdd(p.count + b, 1u);
+      // release: the key merge above before the count; acquire (for the
+      // last arrival): every other chunk's merge
+      const unsigned done = atom_add_acq_rel_u32(p.count + b, 1u);
       if (done >= total) atomicOr(p.err, PE_ERR_WORKSPACE);  // did not start at zero
       const bool last = done == total - 1u;
-      if (last) fence_acq_rel();  // acquire: every chunk of the request is in
       sh.last = last ? b : -1;
     }
   }
@@ -488,8 +488,8 @@ __device__ __forceinline__ void argmax_unit_early(const StepParams& p, SharedSta
     if (tid == 0) {
       int due = -1, a = -1;
       atomicMax(p.keys + r, k);
-      fence_acq_rel();  // release
-      const unsigned rc = atomicAdd(p.rcount + r, 1u);
+      // release / acquire as for the fused step's request count
+      const unsigned rc = atom_add_acq_rel_u32(p.rcount + r, 1u);
       if (rc >= (unsigned)p.C) atomicOr(p.err, PE_ERR_WORKSPACE);  // did not start at zero
       // A chunk whose key beats the draft's own key proves the row's argmax
       // is not the draft: the request mismatches at row j at the latest, so
@@ -508,8 +508,9 @@ __device__ __forceinline__ void argmax_unit_early(const StepParams& p, SharedSta
         const int vb = seg_begin(p, b + 1) - io - 1 - p.Kp;
         const bool match = j < p.Kp && am == __ldg(p.in_tokens + io + vb + j + 1);
         const unsigned long long bits = (1ull << j) | (match ? (1ull << (32 + j)) : 0ull);
-        fence_acq_rel();  // release: the row's argmax before its done bit
-        const unsigned long long old = atomicOr(p.state + b, bits);
+        // release: the row's argmax before its done bit; acquire (for the
+        // CTA that settles the request): the argmax of every row it settles on
+        const unsigned long long old = atom_or_acq_rel(p.state + b, bits);
         // before this OR: done bits of other rows < K'+1 only, match bits of
         // rows < K' only, and not this row's done bit
         const unsigned long long legal =
@@ -518,7 +519,6 @@ __device__ __forceinline__ void argmax_unit_early(const StepParams& p, SharedSta
         if ((old & ~legal) || ((old >> j) & 1ull)) atomicOr(p.err, PE_ERR_WORKSPACE);
         const int a_new = settled(old | bits, p.Kp);
         if (settled(old, p.Kp) < 0 && a_new >= 0) {
-          fence_acq_rel();  // acquire: the argmax of every row it settles on
           due = b;
           a = a_new;
         }
@@ -943,11 +943,11 @@ __global__ void __launch_bounds__(kThreads, 4) step_kernel_early(const StepParam
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    fence_acq_rel();  // release
-    const unsigned done = atomicAdd(p.sched + 1, 1u);
+    // release: this CTA's accesses before its departure; acquire (for the
+    // last to leave): every other CTA's
+    const unsigned done = atom_add_acq_rel_u32(p.sched + 1, 1u);
     if (done > gridDim.x - 1u) atomicOr(p.err, PE_ERR_WORKSPACE);  // did not start at zero
     sh.last = done == gridDim.x - 1;  // every other CTA has left
-    if (sh.last) fence_acq_rel();  // acquire: their last accesses come first
   }
   __syncthreads();
   if (sh.last) {  // the last CTA clears partly read rows, states and row results
