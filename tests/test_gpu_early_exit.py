@@ -134,3 +134,38 @@ def test_kp_above_31_rejected():
     out, ws, err = harness.allocate(w)
     with pytest.raises(_native.PEError):
         harness.run(w, out, ws, err, early_exit=True)
+
+
+def test_early_mismatch_edges():
+    """Rows where a chunk can tell the row's argmax is not the draft before
+    the row completes, and rows where it must not: a draft outside the
+    vocabulary (never the argmax), the row maximum repeated at a column
+    below the draft (the argmax is that column: a mismatch) and above it
+    (the draft keeps the argmax).  Each row spans two chunks, so a chunk can
+    end before its row completes."""
+    spec = wl.SPECS["decode_b256"].with_(B=48, V=60011, row_pad=5, H=64)
+    w = wl.make_workload(spec, 77)
+    nr = w.Kp + 1
+    g = torch.Generator().manual_seed(5)
+    acc = w.planted_accept.tolist()
+    for b in range(w.B):
+        a = int(acc[b])
+        kind = b % 4
+        if a == 0 or kind == 0:
+            continue
+        j = int(torch.randint(0, a, (1,), generator=g))  # a matching row
+        row = b * nr + j
+        d = int(w.in_tokens[b * nr + j + 1])
+        if kind == 1:    # the draft outside the vocabulary: a mismatch at row j
+            w.in_tokens[b * nr + j + 1] = w.V + 5 if b % 8 == 1 else -3
+        elif kind == 2:  # the maximum also at a lower column: a mismatch
+            if d > 0:
+                w.logits[row, d - 1 - int(torch.randint(0, d, (1,), generator=g))] = w.logits[row, d]
+        else:            # the maximum also at a higher column: still a match
+            if d < w.V - 1:
+                c = d + 1 + int(torch.randint(0, w.V - 1 - d, (1,), generator=g))
+                w.logits[row, c] = w.logits[row, d]
+    wg = w.to("cuda")
+    ref = oracle_of(wg)
+    got, _ = run_early(wg)
+    check_early(wg, got, ref)
